@@ -1,0 +1,330 @@
+// C ABI of the DSA hot path: argument validation, workspace sizing, kernel
+// dispatch and the device status word.  See include/dsa.h for the contract.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "dsa_common.cuh"
+
+namespace dsa {
+
+int launch_topk(const Shape& s, const float* scores, long long ld, long long row_begin,
+                long long rows, int32_t* idx, DevCtx c, cudaStream_t st);
+int launch_simt_indexer(const Shape& s, bool bf16, const void* q_I, const void* k_I, const void* w,
+                        long long row_begin, long long rows, float* scores, long long ld, int fill,
+                        DevCtx c, cudaStream_t st);
+int launch_simt_attn_fwd(const Shape& s, bool bf16, const void* q, const void* kv,
+                         const int32_t* idx, void* out, float* mx, float* sm, DevCtx c,
+                         cudaStream_t st);
+int launch_simt_attn_bwd(const Shape& s, bool bf16, const void* q, const void* kv,
+                         const int32_t* idx, const void* out, const void* dout, const float* mx,
+                         const float* sm, void* dq, float* dkv, DevCtx c, cudaStream_t st);
+int launch_simt_kl_bwd(const Shape& s, bool bf16, const void* q, const void* kv, const void* q_I,
+                       const void* k_I, const void* w, const int32_t* idx, const float* mx,
+                       const float* sm, float* loss, void* dq_I, float* dk_I, float* dw, DevCtx c,
+                       cudaStream_t st);
+size_t simt_smem_attn_fwd(const Shape& s);
+size_t simt_smem_attn_bwd(const Shape& s);
+size_t simt_smem_kl(const Shape& s);
+int launch_indexer_tc(const Shape& s, const void* q_I, const void* k_I, const void* w,
+                      long long row_begin, long long rows, float* scores, long long ld, DevCtx c,
+                      cudaStream_t st);
+int launch_attn_fwd_tc(const Shape& s, const void* q, const void* kv, const int32_t* idx, void* out,
+                       float* mx, float* sm, DevCtx c, cudaStream_t st);
+
+// ------------------------------ status word --------------------------------
+__device__ int g_status;
+static unsigned long long g_budget_ns = 2000000000ull;
+static int* g_status_ptr[64];
+
+static bool dev_ctx(DevCtx* c) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return false;
+    g_status_ptr[dev] = (int*)p;
+  }
+  c->status = g_status_ptr[dev];
+  c->budget = g_budget_ns;
+  return true;
+}
+
+// ------------------------------ tensor maps --------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)p;
+  }
+  return fn;
+}
+
+bool make_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
+                       uint32_t box_cols, uint32_t box_rows, int swizzle_bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                          : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                : CU_TENSOR_MAP_SWIZZLE_NONE;
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------ validation ---------------------------------
+static bool aligned16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
+
+static bool tc_attn_shape(const dsa_params* p) { return p->H == 128 && p->d_qk == 576 && p->d_v == 512; }
+static bool tc_indexer_shape(const dsa_params* p) { return p->H_I == 64 && p->d_I == 128; }
+
+static int check_params(const dsa_params* p, Shape* s) {
+  if (!p) return DSA_ERR_INVALID_ARG;
+  if (p->layout != DSA_BSND && p->layout != DSA_TND) return DSA_ERR_UNSUPPORTED;
+  if (p->cp_mode != DSA_CP_COLOSSAL) return DSA_ERR_UNSUPPORTED;
+  if (p->dtype != DSA_BF16 && p->dtype != DSA_FP32) return DSA_ERR_UNSUPPORTED;
+  if (p->B < 1 || p->S_q < 1 || p->S_k < 1 || p->H < 1 || p->d_qk < 1 || p->d_v < 1 ||
+      p->H_I < 1 || p->d_I < 1 || p->topk < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (p->layout == DSA_TND && p->B != 1) return DSA_ERR_INVALID_ARG;
+  if (p->d_v > p->d_qk) return DSA_ERR_INVALID_ARG;
+  if (!(p->scale > 0.f) || !isfinite(p->scale)) return DSA_ERR_INVALID_ARG;
+  if (p->S_k > (1ll << 30) || p->S_q > (1ll << 30) || p->B * p->S_q * p->H >= (1ll << 31) ||
+      p->B * p->S_k >= (1ll << 31) || p->topk > (1 << 20))
+    return DSA_ERR_UNSUPPORTED;
+  if (!p->q_row_index && (p->q_row_offset < 0 || p->q_row_offset + p->S_q > p->S_k))
+    return DSA_ERR_INVALID_ARG;
+  if (p->dtype == DSA_FP32 &&
+      (p->H > 1024 || p->d_qk > 1024 || p->H_I > 256 || p->d_I > 512 || p->topk > 8192))
+    return DSA_ERR_UNSUPPORTED;
+  s->B = (int)p->B;
+  s->S_q = (int)p->S_q;
+  s->S_k = (int)p->S_k;
+  s->H = (int)p->H;
+  s->d_qk = (int)p->d_qk;
+  s->d_v = (int)p->d_v;
+  s->H_I = (int)p->H_I;
+  s->d_I = (int)p->d_I;
+  s->topk = (int)p->topk;
+  s->scale = p->scale;
+  s->q_row_offset = p->q_row_offset;
+  s->q_row_index = p->q_row_index;
+  return DSA_OK;
+}
+
+static int indexer_rows(const dsa_params* p, const Shape& s, const void* q_I, const void* k_I,
+                        const void* w, long long row_begin, long long rows, float* scores,
+                        long long ld, bool fill, DevCtx c, cudaStream_t st) {
+  const bool bf16 = p->dtype == DSA_BF16;
+  if (bf16 && tc_indexer_shape(p)) {
+    if (fill) {  // the tensor-core kernel writes causal keys only: pre-fill the rest
+      int rc = launch_simt_indexer(s, true, q_I, k_I, w, row_begin, rows, scores, ld, 2, c, st);
+      if (rc) return rc;
+    }
+    return launch_indexer_tc(s, q_I, k_I, w, row_begin, rows, scores, ld, c, st);
+  }
+  if (bf16 && (size_t)s.H_I * s.d_I * 4 > 96 * 1024) return DSA_ERR_UNSUPPORTED;
+  return launch_simt_indexer(s, bf16, q_I, k_I, w, row_begin, rows, scores, ld, fill ? 1 : 0, c, st);
+}
+
+static int attn_fwd_supported(const dsa_params* p, const Shape& s, const void* q, const void* kv) {
+  if (p->dtype == DSA_BF16) {
+    if (!tc_attn_shape(p)) return DSA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(kv)) return DSA_ERR_INVALID_ARG;
+    return DSA_OK;
+  }
+  return simt_smem_attn_fwd(s) > 200 * 1024 ? DSA_ERR_UNSUPPORTED : DSA_OK;
+}
+
+static int attn_fwd(const dsa_params* p, const Shape& s, const void* q, const void* kv,
+                    const int32_t* idx, void* out, float* mx, float* sm, DevCtx c, cudaStream_t st) {
+  if (p->dtype == DSA_BF16) return launch_attn_fwd_tc(s, q, kv, idx, out, mx, sm, c, st);
+  return launch_simt_attn_fwd(s, false, q, kv, idx, out, mx, sm, c, st);
+}
+
+static long long wave_rows(const dsa_params* p) {
+  const long long total = p->B * p->S_q;
+  long long w = p->wave_rows;
+  if (w <= 0) {
+    w = (256ll << 20) / (4 * p->S_k);
+    if (w < 1024) w = 1024;
+  }
+  w = (w + 3) / 4 * 4;
+  return w < total ? w : total;
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+int dsa_version(void) { return 100; }
+
+size_t dsa_workspace_size(const dsa_params* p, int which) {
+  Shape s;
+  if (check_params(p, &s) != DSA_OK) return 0;
+  if (which == DSA_CALL_FORWARD) return (size_t)wave_rows(p) * (size_t)p->S_k * sizeof(float);
+  return 0;
+}
+
+int dsa_indexer_scores(const dsa_params* p, const void* q_I, const void* k_I, const void* w,
+                       int64_t row_begin, int64_t rows, float* scores, dsa_stream_t stream) {
+  Shape s;
+  int rc = check_params(p, &s);
+  if (rc) return rc;
+  if (!q_I || !k_I || !w || !scores) return DSA_ERR_INVALID_ARG;
+  if (row_begin < 0 || rows < 1 || row_begin + rows > p->B * p->S_q) return DSA_ERR_INVALID_ARG;
+  if (p->dtype == DSA_BF16 && (!aligned16(q_I) || !aligned16(k_I))) return DSA_ERR_INVALID_ARG;
+  DevCtx c;
+  if (!dev_ctx(&c)) return DSA_ERR_CUDA;
+  return indexer_rows(p, s, q_I, k_I, w, row_begin, rows, scores, p->S_k, true, c,
+                      (cudaStream_t)stream);
+}
+
+int dsa_topk(const dsa_params* p, const float* scores, int64_t row_begin, int64_t rows,
+             int32_t* idx, dsa_stream_t stream) {
+  Shape s;
+  int rc = check_params(p, &s);
+  if (rc) return rc;
+  if (!scores || !idx) return DSA_ERR_INVALID_ARG;
+  if (row_begin < 0 || rows < 1 || row_begin + rows > p->B * p->S_q) return DSA_ERR_INVALID_ARG;
+  DevCtx c;
+  if (!dev_ctx(&c)) return DSA_ERR_CUDA;
+  return launch_topk(s, scores, p->S_k, row_begin, rows, idx, c, (cudaStream_t)stream);
+}
+
+int dsa_sparse_attn_fwd(const dsa_params* p, const void* q, const void* kv, const int32_t* idx,
+                        void* out, float* softmax_max, float* softmax_sum, void* workspace,
+                        dsa_stream_t stream) {
+  (void)workspace;
+  Shape s;
+  int rc = check_params(p, &s);
+  if (rc) return rc;
+  if (!q || !kv || !idx || !out || !softmax_max || !softmax_sum) return DSA_ERR_INVALID_ARG;
+  rc = attn_fwd_supported(p, s, q, kv);
+  if (rc) return rc;
+  DevCtx c;
+  if (!dev_ctx(&c)) return DSA_ERR_CUDA;
+  return attn_fwd(p, s, q, kv, idx, out, softmax_max, softmax_sum, c, (cudaStream_t)stream);
+}
+
+int dsa_sparse_attn_bwd(const dsa_params* p, const void* q, const void* kv, const int32_t* idx,
+                        const void* out, const void* dout, const float* softmax_max,
+                        const float* softmax_sum, void* dq, float* dkv, void* workspace,
+                        dsa_stream_t stream) {
+  (void)workspace;
+  Shape s;
+  int rc = check_params(p, &s);
+  if (rc) return rc;
+  if (!q || !kv || !idx || !out || !dout || !softmax_max || !softmax_sum || !dq || !dkv)
+    return DSA_ERR_INVALID_ARG;
+  if (simt_smem_attn_bwd(s) > 200 * 1024) return DSA_ERR_UNSUPPORTED;
+  DevCtx c;
+  if (!dev_ctx(&c)) return DSA_ERR_CUDA;
+  return launch_simt_attn_bwd(s, p->dtype == DSA_BF16, q, kv, idx, out, dout, softmax_max,
+                              softmax_sum, dq, dkv, c, (cudaStream_t)stream);
+}
+
+int dsa_indexer_kl_loss_bwd(const dsa_params* p, const void* q, const void* kv, const void* q_I,
+                            const void* k_I, const void* w, const int32_t* idx,
+                            const float* softmax_max, const float* softmax_sum, float* loss,
+                            void* dq_I, float* dk_I, float* dw, void* workspace,
+                            dsa_stream_t stream) {
+  (void)workspace;
+  Shape s;
+  int rc = check_params(p, &s);
+  if (rc) return rc;
+  if (!q || !kv || !q_I || !k_I || !w || !idx || !softmax_max || !softmax_sum || !loss || !dq_I ||
+      !dk_I || !dw)
+    return DSA_ERR_INVALID_ARG;
+  if (simt_smem_kl(s) > 200 * 1024) return DSA_ERR_UNSUPPORTED;
+  DevCtx c;
+  if (!dev_ctx(&c)) return DSA_ERR_CUDA;
+  return launch_simt_kl_bwd(s, p->dtype == DSA_BF16, q, kv, q_I, k_I, w, idx, softmax_max,
+                            softmax_sum, loss, dq_I, dk_I, dw, c, (cudaStream_t)stream);
+}
+
+int dsa_forward(const dsa_params* p, const void* q_I, const void* k_I, const void* w,
+                const void* q, const void* kv, int32_t* idx_out, void* out, float* softmax_max,
+                float* softmax_sum, void* workspace, dsa_stream_t stream) {
+  Shape s;
+  int rc = check_params(p, &s);
+  if (rc) return rc;
+  if (!q_I || !k_I || !w || !q || !kv || !idx_out || !out || !softmax_max || !softmax_sum)
+    return DSA_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return DSA_ERR_WORKSPACE;
+  rc = attn_fwd_supported(p, s, q, kv);
+  if (rc) return rc;
+  if (p->dtype == DSA_BF16 && (!aligned16(q_I) || !aligned16(k_I))) return DSA_ERR_INVALID_ARG;
+  DevCtx c;
+  if (!dev_ctx(&c)) return DSA_ERR_CUDA;
+  cudaStream_t st = (cudaStream_t)stream;
+  const long long total = p->B * p->S_q, W = wave_rows(p);
+  float* ring = (float*)workspace;
+  for (long long r0 = 0; r0 < total; r0 += W) {
+    const long long n = (total - r0) < W ? (total - r0) : W;
+    rc = indexer_rows(p, s, q_I, k_I, w, r0, n, ring, p->S_k, false, c, st);
+    if (rc) return rc;
+    rc = launch_topk(s, ring, p->S_k, r0, n, idx_out + r0 * p->topk, c, st);
+    if (rc) return rc;
+  }
+  return attn_fwd(p, s, q, kv, idx_out, out, softmax_max, softmax_sum, c, st);
+}
+
+int dsa_get_status(dsa_stream_t stream, int* device_status) {
+  if (!device_status) return DSA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DSA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return DSA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return DSA_ERR_CUDA;
+  *device_status = v;
+  return DSA_OK;
+}
+
+int dsa_set_wait_budget_ns(uint64_t budget_ns) {
+  if (budget_ns == 0) return DSA_ERR_INVALID_ARG;
+  g_budget_ns = budget_ns;
+  return DSA_OK;
+}
+
+}  // extern "C"
+
+namespace dsa {
+// one warp waits on an mbarrier that nothing completes; the bounded wait gives
+// up after the budget and records DSA_ERR_TIMEOUT.
+__global__ void selftest_wait_kernel(DevCtx c) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait(smem_u32(&bar), 0, c, &abort_flag);
+}
+}  // namespace dsa
+
+extern "C" int dsa_selftest_wait_timeout(uint64_t budget_ns, dsa_stream_t stream) {
+  if (budget_ns == 0 || budget_ns > 10000000000ull) return DSA_ERR_INVALID_ARG;
+  DevCtx c;
+  if (!dev_ctx(&c)) return DSA_ERR_CUDA;
+  c.budget = budget_ns;
+  selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(c);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}

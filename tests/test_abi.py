@@ -1,0 +1,71 @@
+"""The C-ABI library builds, loads without a GPU, and exports every entry
+point include/dsa.h declares (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    import sparse_attention_long_gb300 as dsa
+    return dsa
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_path():
+    names = declared_symbols()
+    for n in ["dsa_indexer_scores", "dsa_topk", "dsa_sparse_attn_fwd", "dsa_sparse_attn_bwd",
+              "dsa_forward", "dsa_indexer_kl_loss_bwd", "dsa_get_status", "dsa_workspace_size"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    dsa = _lib()
+    raw = ctypes.CDLL(dsa.LIB_PATH)
+    for n in declared_symbols():
+        assert hasattr(raw, n), n
+    assert dsa.version() == 100
+
+
+def test_params_struct_layout_matches_header():
+    dsa = _lib()
+    # 4 int32, 9 int64, float + int32, int64, pointer, int64
+    assert ctypes.sizeof(dsa.dsa_params) == 16 + 9 * 8 + 8 + 8 + 8 + 8
+
+
+def test_host_validation_without_gpu():
+    # argument errors are found on the host before any CUDA call
+    dsa = _lib()
+    p = dsa.make_params(B=1, S_q=8, S_k=8, H=2, d_qk=8, d_v=4, H_I=2, d_I=4, topk=4, scale=0.5,
+                        dtype="fp32")
+    assert dsa.workspace_size(p, dsa.DSA_CALL_FORWARD) == 8 * 8 * 4
+    bad = dsa.make_params(B=1, S_q=8, S_k=8, H=2, d_qk=8, d_v=16, H_I=2, d_I=4, topk=4, scale=0.5,
+                          dtype="fp32")
+    assert dsa.lib.dsa_sparse_attn_fwd(ctypes.byref(bad), 16, 16, 16, 16, 16, 16, None, None) == \
+        dsa.DSA_ERR_INVALID_ARG
+    uly = dsa.make_params(B=1, S_q=8, S_k=8, H=2, d_qk=8, d_v=4, H_I=2, d_I=4, topk=4, scale=0.5,
+                          dtype="fp32", cp_mode="ulysses")
+    assert dsa.lib.dsa_topk(ctypes.byref(uly), 16, 0, 1, 16, None) == dsa.DSA_ERR_UNSUPPORTED
+    tnd = dsa.make_params(B=2, S_q=8, S_k=8, H=2, d_qk=8, d_v=4, H_I=2, d_I=4, topk=4, scale=0.5,
+                          dtype="fp32", layout="TND")
+    assert dsa.lib.dsa_topk(ctypes.byref(tnd), 16, 0, 1, 16, None) == dsa.DSA_ERR_INVALID_ARG
+    off = dsa.make_params(B=1, S_q=8, S_k=8, H=2, d_qk=8, d_v=4, H_I=2, d_I=4, topk=4, scale=0.5,
+                          dtype="fp32", q_row_offset=1)
+    assert dsa.lib.dsa_topk(ctypes.byref(off), 16, 0, 1, 16, None) == dsa.DSA_ERR_INVALID_ARG
+    assert dsa.lib.dsa_topk(ctypes.byref(p), 16, 0, 9, 16, None) == dsa.DSA_ERR_INVALID_ARG
+    assert dsa.lib.dsa_topk(None, 16, 0, 1, 16, None) == dsa.DSA_ERR_INVALID_ARG
+    bf = dsa.make_params(B=1, S_q=8, S_k=8, H=64, d_qk=576, d_v=512, H_I=64, d_I=128, topk=4,
+                         scale=0.5, dtype="bf16")
+    assert dsa.lib.dsa_sparse_attn_fwd(ctypes.byref(bf), 16, 16, 16, 16, 16, 16, None, None) == \
+        dsa.DSA_ERR_UNSUPPORTED

@@ -1,0 +1,135 @@
+"""bf16 tensor-core path at the DeepSeek-V3.2 head shapes (128 heads,
+d_qk=576, d_v=512, indexer 64x128) against the fp64 oracle on the same
+bf16-rounded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import (DEV, SCORE_MAXABS, bf16_close, empty_outputs, lib, near_tie_violations,
+                      np64, params)
+
+pytestmark = pytest.mark.gpu
+
+
+def _wl(S, k):
+    return dict(synth.v32(S, f"dsv32_S{S}"), topk=k)
+
+
+@pytest.fixture(scope="module")
+def small():
+    wl = _wl(448, 200)    # several 128-key blocks, ragged tails, k not a multiple of 64
+    return wl, synth.make_inputs(wl)
+
+
+def test_indexer_scores_small(small):
+    dsa = lib()
+    wl, x = small
+    S = wl["S"]
+    p = params(dsa, wl)
+    sc = torch.empty(S, S, device=DEV)
+    g = {k: v.to(DEV) for k, v in x.items()}
+    dsa.indexer_scores(p, g["q_I"], g["k_I"], g["w"], 0, S, sc)
+    torch.cuda.synchronize()
+    assert dsa.get_status() == 0
+    ref = oracle.indexer_scores(x["q_I"], x["k_I"], x["w"], oracle.positions(1, S))[0]
+    got = np64(sc)
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(got), fin)
+    err = np.abs(got[fin] - ref[fin])
+    assert err.max() < SCORE_MAXABS, err.max()
+
+
+def test_indexer_row_window(small):
+    # a window of rows written at the start of the output (row_begin > 0)
+    dsa = lib()
+    wl, x = small
+    S = wl["S"]
+    p = params(dsa, wl)
+    g = {k: v.to(DEV) for k, v in x.items()}
+    full = torch.empty(S, S, device=DEV)
+    dsa.indexer_scores(p, g["q_I"], g["k_I"], g["w"], 0, S, full)
+    part = torch.empty(37, S, device=DEV)
+    dsa.indexer_scores(p, g["q_I"], g["k_I"], g["w"], 301, 37, part)
+    torch.cuda.synchronize()
+    assert torch.equal(part, full[301:338])
+
+
+def test_attention_small_on_oracle_indices(small):
+    dsa = lib()
+    wl, x = small
+    S, k = wl["S"], wl["topk"]
+    pos = oracle.positions(1, S)
+    sc = oracle.indexer_scores(x["q_I"], x["k_I"], x["w"], pos)
+    ridx = oracle.topk_select(sc, pos, k)
+    # also exercise -1 holes and a shuffled order inside some rows
+    rng = np.random.default_rng(0)
+    for r in range(0, S, 7):
+        row = ridx[0, r].copy()
+        rng.shuffle(row)
+        ridx[0, r] = row
+    O, m, l = oracle.sparse_attn_fwd(x["q"], x["kv"], ridx, wl["scale"], 512)
+    p = params(dsa, wl)
+    o = empty_outputs(wl, S, torch.bfloat16)
+    dsa.sparse_attn_fwd(p, x["q"].to(DEV), x["kv"].to(DEV), torch.as_tensor(ridx, device=DEV),
+                        o["out"], o["m"], o["l"])
+    torch.cuda.synchronize()
+    assert dsa.get_status() == 0
+    ok, ma, mr = bf16_close(np64(o["out"]), O)
+    assert ok, (ma, mr)
+    assert np.abs(np64(o["m"]) - m).max() < 1e-4
+    assert (np.abs(np64(o["l"]) - l) / l).max() < 1e-4
+
+
+def test_forward_c2_sampled_rows():
+    # S = 4096, top-2048: every stage at the pages' head shapes; oracle on sampled rows
+    dsa = lib()
+    wl = synth.WORKLOADS["dsv32_S4096"]
+    S, k = wl["S"], wl["topk"]
+    x = synth.make_inputs(wl, device=DEV)
+    p = params(dsa, wl)
+    o = empty_outputs(wl, S, torch.bfloat16)
+    ws = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_FORWARD) // 4, device=DEV)
+    dsa.forward(p, x["q_I"], x["k_I"], x["w"], x["q"], x["kv"], o["idx"], o["out"], o["m"], o["l"], ws)
+    torch.cuda.synchronize()
+    assert dsa.get_status() == 0
+    rows = np.unique(np.concatenate([np.arange(0, 8), np.arange(S - 8, S),
+                                     np.random.default_rng(1).integers(0, S, 48), [2046, 2047, 2048]]))
+    xc = {n: v[:, rows].cpu() if n in ("q_I", "w", "q") else v.cpu() for n, v in x.items()}
+    pos = oracle.positions(1, S)[:, rows]
+    sc = oracle.indexer_scores(xc["q_I"], xc["k_I"], xc["w"], pos)
+    ridx = oracle.topk_select(sc, pos, k)
+    gi = o["idx"].cpu().numpy()[0, rows]
+    assert near_tie_violations(gi, ridx[0], sc[0], k) == []
+    O, m, l = oracle.sparse_attn_fwd(xc["q"], xc["kv"], ridx, wl["scale"], 512)
+    same = [i for i in range(rows.size) if set(gi[i]) == set(ridx[0, i])]
+    assert len(same) >= rows.size // 2
+    ok, ma, mr = bf16_close(np64(o["out"])[0, rows][same], O[0, same])
+    assert ok, (ma, mr)
+
+
+def test_cp_head_tail_shard_bit_identical():
+    # CP degree 4, head-tail rows of rank 0 at S = 4096 against the unsharded run
+    dsa = lib()
+    wl = synth.WORKLOADS["dsv32_S4096"]
+    S = wl["S"]
+    x = synth.make_inputs(wl, device=DEV)
+
+    def run(rows, **kw):
+        n = len(rows)
+        p = params(dsa, wl, S_q=n, **kw)
+        o = empty_outputs(wl, n, torch.bfloat16)
+        ws = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_FORWARD) // 4, device=DEV)
+        dsa.forward(p, x["q_I"][:, rows].contiguous(), x["k_I"], x["w"][:, rows].contiguous(),
+                    x["q"][:, rows].contiguous(), x["kv"], o["idx"], o["out"], o["m"], o["l"], ws)
+        torch.cuda.synchronize()
+        return o
+
+    full = run(list(range(S)))
+    rows = synth.head_tail_rows(S, 4, 0)
+    ht = run(rows.tolist(), q_row_index=torch.as_tensor(rows, device=DEV))
+    off = run(list(range(1024, 2048)), q_row_offset=1024)
+    for part, rr in ((ht, rows.tolist()), (off, list(range(1024, 2048)))):
+        for key in ("idx", "out", "m", "l"):
+            assert torch.equal(part[key], full[key][:, rr]), key
