@@ -1,0 +1,389 @@
+#!/usr/bin/env python3
+"""DSA forward benchmark on GB300: query tokens/s at S = 32768, top-2048
+(DeepSeek-V3.2 shapes: 128 heads, d_qk 576, d_v 512, indexer 64 x 128), plus
+the tensor-core fraction of the indexer + attention stages.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one pass of the whole hot path over one synthetic batch: indexer
+scores -> top-k (streamed in row waves through a workspace ring) -> sparse
+attention, through the library's C ABI.  N > 1 (torchrun): every rank runs an
+independent replica problem of its own (weak scaling, no collective on the
+data path); value = all ranks' tokens / the slowest rank's time.
+
+--impl reference times the CPU oracle (numpy fp64) on the host cores on a
+bounded sample of query rows of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "DSA fwd query tokens/s @S=32K top-2048; % of GB300 bf16 tensor-core peak"
+UNIT = "query tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["source"] = "fallback"
+    return d
+
+
+def algorithmic(wl, pos):
+    """Work the method must do (causal / selected pairs only)."""
+    n = pos.astype(np.float64) + 1.0
+    sel = np.minimum(n, wl["topk"])
+    f_idx = 2.0 * wl["H_I"] * wl["d_I"] * n.sum()
+    f_attn = 2.0 * wl["H"] * (wl["d_qk"] + wl["d_v"]) * sel.sum()
+    topk_bytes = 4.0 * n.sum() + 4.0 * wl["topk"] * pos.size
+    return f_idx, f_attn, topk_bytes
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_traffic(kernel_file, summary):
+    """DRAM bytes per launch recorded by an ncu capture, valid only while the
+    kernel source is unchanged (sha256 prefix recorded beside the number)."""
+    path = os.path.join(ROOT, "profiles", summary)
+    src = os.path.join(ROOT, "sparse_attention_long_gb300", "csrc", kernel_file)
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_sha256")):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_sha256") != h:
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ oracle arm
+def oracle_inputs(wl, rows, seed=0):
+    """The workload's inputs restricted to the sampled query rows (the
+    generator is counter based, so rows are drawn directly)."""
+    S, H, dqk, HI, dI = wl["S"], wl["H"], wl["d_qk"], wl["H_I"], wl["d_I"]
+
+    def rows_of(name, width, scale):
+        parts = [synth.normal_flat(int(t) * width, width, seed, synth.STREAM[name]) for t in rows]
+        return (torch.stack(parts) * scale).to(torch.bfloat16)
+
+    return dict(q_I=rows_of("q_I", HI * dI, 1.0).view(1, len(rows), HI, dI),
+                w=rows_of("w", HI, 1.0 / 8).view(1, len(rows), HI),
+                q=rows_of("q", H * dqk, 1.0).view(1, len(rows), H, dqk),
+                k_I=synth.normal((1, S, dI), "k_I", seed),
+                kv=synth.normal((1, S, dqk), "kv", seed))
+
+
+def oracle_step(wl, x, rows):
+    import oracle
+    pos = np.asarray(rows, dtype=np.int64)[None]
+    sc = oracle.indexer_scores(x["q_I"], x["k_I"], x["w"], pos)
+    idx = oracle.topk_select(sc, pos, wl["topk"])
+    oracle.sparse_attn_fwd(x["q"], x["kv"], idx, wl["scale"], wl["d_v"])
+
+
+def sample_rows(S, n, seed=0):
+    rng = np.random.default_rng(seed)
+    a = max(1, n // 4)
+    rows = np.concatenate([np.arange(a), np.arange(S - a, S), rng.integers(0, S, n - 2 * a)])
+    return np.unique(rows)[:n]
+
+
+def cpu_baseline(wl, budget_s=15.0):
+    """The oracle as it stands, on the host cores, on sampled query rows."""
+    rows_all = sample_rows(wl["S"], 2048, seed=0)
+    x = oracle_inputs(wl, rows_all)
+    done, t0 = 0, time.perf_counter()
+    while done < rows_all.size and time.perf_counter() - t0 < budget_s:
+        chunk = list(range(done, min(done + 8, rows_all.size)))
+        xs = dict(x, q_I=x["q_I"][:, chunk], w=x["w"][:, chunk], q=x["q"][:, chunk])
+        oracle_step(wl, xs, rows_all[chunk])
+        done += len(chunk)
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": done / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done} query rows of the S={wl['S']} workload (first/last/uniform), "
+                      f"indexer over all causal keys + top-k + attention, numpy fp64, {dt:.1f} s"}
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    rows_per_step = 8
+    rows_all = sample_rows(wl["S"], rows_per_step * (args.steps + args.warmup), seed=1)
+    x = oracle_inputs(wl, rows_all)
+    times = []
+    for i in range(args.warmup + args.steps):
+        chunk = list(range(i * rows_per_step, min((i + 1) * rows_per_step, rows_all.size)))
+        if not chunk:
+            chunk = list(range(rows_per_step))
+        xs = dict(x, q_I=x["q_I"][:, chunk], w=x["w"][:, chunk], q=x["q"][:, chunk])
+        t0 = time.perf_counter()
+        oracle_step(wl, xs, rows_all[chunk])
+        if i >= args.warmup:
+            times.append((time.perf_counter() - t0, len(chunk)))
+    tot = sum(t for t, _ in times)
+    value = sum(n for _, n in times) / tot
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot / len(times), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl["name"], "S": wl["S"], "topk": wl["topk"],
+                       "rows_per_step": rows_per_step},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{rows_per_step} query rows per step of the S={wl['S']} "
+                                       "workload, numpy fp64 on the host cores"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- our arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dsv32_S32768", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import sparse_attention_long_gb300 as dsa
+
+    S, k = wl["S"], wl["topk"]
+    x = synth.make_inputs(wl, device=dev, seed=rank)   # each rank: its own replica problem
+    mk = lambda **kw: dsa.make_params(B=1, S_q=S, S_k=S, H=wl["H"], d_qk=wl["d_qk"], d_v=wl["d_v"],
+                                      H_I=wl["H_I"], d_I=wl["d_I"], topk=k, scale=wl["scale"],
+                                      dtype="bf16", **kw)
+    p = mk()
+    p_causal = mk(flags=dsa.DSA_FLAG_CAUSAL_ONLY)
+    W = dsa.wave_rows(p)
+    ring = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_FORWARD) // 4, device=dev)
+    idx = torch.empty(1, S, k, dtype=torch.int32, device=dev)
+    out = torch.empty(1, S, wl["H"], wl["d_v"], dtype=torch.bfloat16, device=dev)
+    m = torch.empty(1, S, wl["H"], device=dev)
+    l = torch.empty_like(m)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    waves = [(r0, min(W, S - r0)) for r0 in range(0, S, W)]
+
+    def step(ev=None):
+        for i, (r0, n) in enumerate(waves):
+            if ev: ev["idx"][i][0].record(stream)
+            dsa.indexer_scores(p_causal, x["q_I"], x["k_I"], x["w"], r0, n, ring)
+            if ev: ev["idx"][i][1].record(stream)
+            dsa.topk(p, ring, r0, n, idx.view(S, k)[r0:r0 + n])
+            if ev: ev["topk"][i][1].record(stream)
+        if ev: ev["attn"][0].record(stream)
+        dsa.sparse_attn_fwd(p, x["q"], x["kv"], idx, out, m, l)
+        if ev: ev["attn"][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    assert dsa.get_status() == 0, "device status after warm-up"
+
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    evs = [dict(idx=[(E(), E()) for _ in waves], topk=[(None, E()) for _ in waves], attn=(E(), E()))
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for s in range(args.steps):
+        step(evs[s])
+        flush.zero_()          # L2 flush between steps (outside the per-stage events)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    assert dsa.get_status() == 0, "device status after the timed steps"
+
+    t_idx = t_topk = t_attn = 0.0
+    for e in evs:
+        for i in range(len(waves)):
+            t_idx += e["idx"][i][0].elapsed_time(e["idx"][i][1])
+            t_topk += e["idx"][i][1].elapsed_time(e["topk"][i][1])
+        t_attn += e["attn"][0].elapsed_time(e["attn"][1])
+    K = args.steps
+    t_idx, t_topk, t_attn = t_idx / K, t_topk / K, t_attn / K      # ms per step
+    ms_step = t_idx + t_topk + t_attn
+    if world > 1:
+        tt = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(tt)
+
+    f_idx, f_attn, topk_bytes = algorithmic(wl, np.arange(S))
+    peaks = load_peaks()
+    peak_tc = peaks["bf16_tflops_sustained"]
+    value = world * S / (ms_step * 1e-3)
+    attn_tflops = f_attn / (t_attn * 1e-3) / 1e12
+    tensor_frac = (f_idx + f_attn) / ((t_idx + t_attn) * 1e-3) / 1e12 / peak_tc
+
+    # end to end through dsa_forward with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = {n: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for n, v in x.items()}
+        for n in host_in:
+            host_in[n].copy_(x[n])
+        host_out = dict(idx=torch.empty(idx.shape, dtype=idx.dtype, pin_memory=True),
+                        out=torch.empty(out.shape, dtype=out.dtype, pin_memory=True),
+                        m=torch.empty(m.shape, pin_memory=True), l=torch.empty(l.shape, pin_memory=True))
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+        def e2e_step():
+            for n in host_in:
+                x[n].copy_(host_in[n], non_blocking=True)
+            dsa.forward(p, x["q_I"], x["k_I"], x["w"], x["q"], x["kv"], idx, out, m, l, ring)
+            host_out["idx"].copy_(idx, non_blocking=True)
+            host_out["out"].copy_(out, non_blocking=True)
+            host_out["m"].copy_(m, non_blocking=True)
+            host_out["l"].copy_(l, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        ke = max(3, K // 2)
+        a, b = E(), E()
+        a.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = a.elapsed_time(b) / ke
+        if world > 1:
+            tt = torch.tensor([ms_e2e], device=dev)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            ms_e2e = float(tt)
+        e2e = {"value": world * S / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
+        assert dsa.get_status() == 0
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(wl)
+    launches_per_step = len(waves) * 2 + 1
+    traffic = kernel_traffic("attn_fwd_tc.cu", "attn_fwd_tc_S32768.md")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl["name"], "B": 1, "S": S, "topk": k, "H": wl["H"],
+                   "d_qk": wl["d_qk"], "d_v": wl["d_v"], "H_I": wl["H_I"], "d_I": wl["d_I"],
+                   "wave_rows": W, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (q 4.8 GB) and a 256 MiB L2 flush between steps"},
+        "roofline": {"bound": "tensor", "kernel": "attn_fwd_tc_kernel",
+                     "achieved": attn_tflops, "peak": peak_tc, "unit": "TFLOP/s",
+                     "frac": attn_tflops / peak_tc,
+                     "peak_source": f"{peaks['source']} bf16_tflops_sustained",
+                     "traffic": traffic},
+        "tensor_frac_indexer_plus_attention": tensor_frac,
+        "stages": {"indexer_ms": t_idx, "topk_ms": t_topk, "attention_ms": t_attn,
+                   "indexer_tflops": f_idx / (t_idx * 1e-3) / 1e12,
+                   "attention_tflops": attn_tflops,
+                   "topk_gbs": topk_bytes / (t_topk * 1e-3) / 1e9,
+                   "topk_hbm_frac": topk_bytes / (t_topk * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+        "wall_s_timed": t_wall,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

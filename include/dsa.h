@@ -68,6 +68,10 @@ enum { DSA_BF16 = 0, DSA_FP32 = 1 };
  * "ulysses" is an error there and is DSA_ERR_UNSUPPORTED here. */
 enum { DSA_CP_COLOSSAL = 0, DSA_CP_ULYSSES = 1 };
 
+/* dsa_params.flags: dsa_indexer_scores writes only the causal entries
+ * s <= pos(t) and leaves the rest of each score row untouched. */
+enum { DSA_FLAG_CAUSAL_ONLY = 1 };
+
 /* workspace queries (dsa_workspace_size `which`) */
 enum { DSA_CALL_FORWARD = 0, DSA_CALL_ATTN_FWD = 1, DSA_CALL_ATTN_BWD = 2, DSA_CALL_KL_BWD = 3 };
 
@@ -75,7 +79,7 @@ typedef struct {
   int32_t layout;              /* DSA_BSND or DSA_TND (TND requires B == 1)            */
   int32_t dtype;               /* DSA_BF16 or DSA_FP32                                 */
   int32_t cp_mode;             /* DSA_CP_COLOSSAL (0)                                  */
-  int32_t reserved0;
+  int32_t flags;               /* DSA_FLAG_* bits, 0 = defaults                        */
   int64_t B, S_q, S_k;         /* batch, local query rows, key length (global)         */
   int64_t H, d_qk, d_v;        /* attention heads, q/k width, value width (V = kv[:d_v]) */
   int64_t H_I, d_I;            /* indexer heads and width                              */
@@ -101,7 +105,8 @@ size_t dsa_workspace_size(const dsa_params *p, int which);
  * one index key per position shared by the H_I index heads (MQA).
  *   q_I    [B, S_q, H_I, d_I]   k_I [B, S_k, d_I]   w [B, S_q, H_I]
  *   scores [rows, S_k] fp32 for flattened rows [row_begin, row_begin+rows);
- *          entries s > pos(t) are written as -inf.
+ *          entries s > pos(t) are written as -inf (left untouched with
+ *          DSA_FLAG_CAUSAL_ONLY).
  * rows must not be 0; row_begin + rows <= B*S_q.
  */
 int dsa_indexer_scores(const dsa_params *p, const void *q_I, const void *k_I, const void *w,
@@ -148,6 +153,8 @@ int dsa_sparse_attn_fwd(const dsa_params *p, const void *q, const void *kv, cons
  *   out, dout [B, S_q, H, d_v]   dq [B, S_q, H, d_qk] (written)
  *   dkv [B, S_k, d_qk] fp32: ACCUMULATED (+=) with atomics -- the caller
  *       zeroes it (or passes partial sums of other shards).
+ *   workspace: dsa_workspace_size(p, DSA_CALL_ATTN_BWD) bytes (the fp32 path
+ *       accumulates dkv in fp64 there first; NULL allowed when the size is 0).
  */
 int dsa_sparse_attn_bwd(const dsa_params *p, const void *q, const void *kv, const int32_t *idx,
                         const void *out, const void *dout, const float *softmax_max,
@@ -164,6 +171,8 @@ int dsa_sparse_attn_bwd(const dsa_params *p, const void *q, const void *kv, cons
  *   loss  1 fp32, ACCUMULATED (+= this call's rows); caller zeroes.
  *   dq_I [B, S_q, H_I, d_I] written;  dw [B, S_q, H_I] fp32 written;
  *   dk_I [B, S_k, d_I] fp32 ACCUMULATED with atomics; caller zeroes.
+ *   workspace: dsa_workspace_size(p, DSA_CALL_KL_BWD) bytes (fp32 path: fp64
+ *       accumulation of dk_I; NULL allowed when the size is 0).
  */
 int dsa_indexer_kl_loss_bwd(const dsa_params *p, const void *q, const void *kv, const void *q_I,
                             const void *k_I, const void *w, const int32_t *idx,

@@ -21,6 +21,7 @@ DSA_BSND, DSA_TND = 0, 1
 DSA_BF16, DSA_FP32 = 0, 1
 DSA_CP_COLOSSAL, DSA_CP_ULYSSES = 0, 1
 DSA_CALL_FORWARD, DSA_CALL_ATTN_FWD, DSA_CALL_ATTN_BWD, DSA_CALL_KL_BWD = 0, 1, 2, 3
+DSA_FLAG_CAUSAL_ONLY = 1
 
 _ERRNAMES = {0: "DSA_OK", -1: "DSA_ERR_INVALID_ARG", -2: "DSA_ERR_UNSUPPORTED",
              -3: "DSA_ERR_WORKSPACE", -4: "DSA_ERR_CUDA", -5: "DSA_ERR_TIMEOUT", -6: "DSA_ERR_INDEX"}
@@ -34,7 +35,7 @@ class DSAError(RuntimeError):
 
 class dsa_params(ctypes.Structure):
     _fields_ = [("layout", ctypes.c_int32), ("dtype", ctypes.c_int32), ("cp_mode", ctypes.c_int32),
-                ("reserved0", ctypes.c_int32),
+                ("flags", ctypes.c_int32),
                 ("B", ctypes.c_int64), ("S_q", ctypes.c_int64), ("S_k", ctypes.c_int64),
                 ("H", ctypes.c_int64), ("d_qk", ctypes.c_int64), ("d_v", ctypes.c_int64),
                 ("H_I", ctypes.c_int64), ("d_I", ctypes.c_int64), ("topk", ctypes.c_int64),
@@ -91,7 +92,7 @@ def _stream(stream):
 
 def make_params(*, B, S_q, S_k, H, d_qk, d_v, H_I, d_I, topk, scale, dtype="bf16",
                 layout="BSND", q_row_offset=0, q_row_index=None, wave_rows=0,
-                cp_mode="colossal") -> dsa_params:
+                cp_mode="colossal", flags=0) -> dsa_params:
     """Builds the C parameter block.  ``q_row_index`` is a device int32 tensor
     (kept alive by the caller) or None."""
     p = dsa_params()
@@ -103,7 +104,18 @@ def make_params(*, B, S_q, S_k, H, d_qk, d_v, H_I, d_I, topk, scale, dtype="bf16
     p.q_row_offset = q_row_offset
     p.q_row_index = None if q_row_index is None else _ptr(q_row_index)
     p.wave_rows = wave_rows
+    p.flags = flags
     return p
+
+
+def wave_rows(p: dsa_params) -> int:
+    """Rows per indexer/top-k wave dsa_forward uses (mirrors the library)."""
+    total = p.B * p.S_q
+    w = p.wave_rows
+    if w <= 0:
+        w = max((256 << 20) // (4 * p.S_k), 1024)
+    w = (w + 3) // 4 * 4
+    return min(w, total)
 
 
 def version() -> int:

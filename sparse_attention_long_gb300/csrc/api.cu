@@ -18,11 +18,12 @@ int launch_simt_attn_fwd(const Shape& s, bool bf16, const void* q, const void* k
                          cudaStream_t st);
 int launch_simt_attn_bwd(const Shape& s, bool bf16, const void* q, const void* kv,
                          const int32_t* idx, const void* out, const void* dout, const float* mx,
-                         const float* sm, void* dq, float* dkv, DevCtx c, cudaStream_t st);
+                         const float* sm, void* dq, float* dkv, double* ws, DevCtx c,
+                         cudaStream_t st);
 int launch_simt_kl_bwd(const Shape& s, bool bf16, const void* q, const void* kv, const void* q_I,
                        const void* k_I, const void* w, const int32_t* idx, const float* mx,
-                       const float* sm, float* loss, void* dq_I, float* dk_I, float* dw, DevCtx c,
-                       cudaStream_t st);
+                       const float* sm, float* loss, void* dq_I, float* dk_I, float* dw,
+                       double* ws, DevCtx c, cudaStream_t st);
 size_t simt_smem_attn_fwd(const Shape& s);
 size_t simt_smem_attn_bwd(const Shape& s);
 size_t simt_smem_kl(const Shape& s);
@@ -178,6 +179,11 @@ size_t dsa_workspace_size(const dsa_params* p, int which) {
   Shape s;
   if (check_params(p, &s) != DSA_OK) return 0;
   if (which == DSA_CALL_FORWARD) return (size_t)wave_rows(p) * (size_t)p->S_k * sizeof(float);
+  // the exact (fp32) path accumulates dkv / dk_I in fp64 before adding them
+  if (which == DSA_CALL_ATTN_BWD && p->dtype == DSA_FP32)
+    return (size_t)(p->B * p->S_k * p->d_qk) * sizeof(double);
+  if (which == DSA_CALL_KL_BWD && p->dtype == DSA_FP32)
+    return (size_t)(p->B * p->S_k * p->d_I) * sizeof(double);
   return 0;
 }
 
@@ -191,7 +197,8 @@ int dsa_indexer_scores(const dsa_params* p, const void* q_I, const void* k_I, co
   if (p->dtype == DSA_BF16 && (!aligned16(q_I) || !aligned16(k_I))) return DSA_ERR_INVALID_ARG;
   DevCtx c;
   if (!dev_ctx(&c)) return DSA_ERR_CUDA;
-  return indexer_rows(p, s, q_I, k_I, w, row_begin, rows, scores, p->S_k, true, c,
+  const bool fill = (p->flags & DSA_FLAG_CAUSAL_ONLY) == 0;
+  return indexer_rows(p, s, q_I, k_I, w, row_begin, rows, scores, p->S_k, fill, c,
                       (cudaStream_t)stream);
 }
 
@@ -226,17 +233,17 @@ int dsa_sparse_attn_bwd(const dsa_params* p, const void* q, const void* kv, cons
                         const void* out, const void* dout, const float* softmax_max,
                         const float* softmax_sum, void* dq, float* dkv, void* workspace,
                         dsa_stream_t stream) {
-  (void)workspace;
   Shape s;
   int rc = check_params(p, &s);
   if (rc) return rc;
   if (!q || !kv || !idx || !out || !dout || !softmax_max || !softmax_sum || !dq || !dkv)
     return DSA_ERR_INVALID_ARG;
   if (simt_smem_attn_bwd(s) > 200 * 1024) return DSA_ERR_UNSUPPORTED;
+  if (dsa_workspace_size(p, DSA_CALL_ATTN_BWD) > 0 && !aligned16(workspace)) return DSA_ERR_WORKSPACE;
   DevCtx c;
   if (!dev_ctx(&c)) return DSA_ERR_CUDA;
   return launch_simt_attn_bwd(s, p->dtype == DSA_BF16, q, kv, idx, out, dout, softmax_max,
-                              softmax_sum, dq, dkv, c, (cudaStream_t)stream);
+                              softmax_sum, dq, dkv, (double*)workspace, c, (cudaStream_t)stream);
 }
 
 int dsa_indexer_kl_loss_bwd(const dsa_params* p, const void* q, const void* kv, const void* q_I,
@@ -244,7 +251,6 @@ int dsa_indexer_kl_loss_bwd(const dsa_params* p, const void* q, const void* kv, 
                             const float* softmax_max, const float* softmax_sum, float* loss,
                             void* dq_I, float* dk_I, float* dw, void* workspace,
                             dsa_stream_t stream) {
-  (void)workspace;
   Shape s;
   int rc = check_params(p, &s);
   if (rc) return rc;
@@ -252,10 +258,12 @@ int dsa_indexer_kl_loss_bwd(const dsa_params* p, const void* q, const void* kv, 
       !dk_I || !dw)
     return DSA_ERR_INVALID_ARG;
   if (simt_smem_kl(s) > 200 * 1024) return DSA_ERR_UNSUPPORTED;
+  if (dsa_workspace_size(p, DSA_CALL_KL_BWD) > 0 && !aligned16(workspace)) return DSA_ERR_WORKSPACE;
   DevCtx c;
   if (!dev_ctx(&c)) return DSA_ERR_CUDA;
   return launch_simt_kl_bwd(s, p->dtype == DSA_BF16, q, kv, q_I, k_I, w, idx, softmax_max,
-                            softmax_sum, loss, dq_I, dk_I, dw, c, (cudaStream_t)stream);
+                            softmax_sum, loss, dq_I, dk_I, dw, (double*)workspace, c,
+                            (cudaStream_t)stream);
 }
 
 int dsa_forward(const dsa_params* p, const void* q_I, const void* k_I, const void* w,

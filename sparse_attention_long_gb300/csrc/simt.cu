@@ -148,13 +148,13 @@ __global__ void __launch_bounds__(128)
 
 // [DSA-32K] SparseFlashAttentionGrad.  grid (H, rows), block 128.
 // dkv gets fp32 atomics per (head, key, column): small shapes only.
-template <typename T>
+template <typename T, typename A>
 __global__ void __launch_bounds__(128)
     simt_attn_bwd_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ kv,
                          const int32_t* __restrict__ idx, const T* __restrict__ out,
                          const T* __restrict__ dout, const float* __restrict__ mx,
                          const float* __restrict__ sm_in, T* __restrict__ dq,
-                         float* __restrict__ dkv, DevCtx c) {
+                         A* __restrict__ dkv, DevCtx c) {
   extern __shared__ float sh[];
   float* qh = sh;                // [d_qk]
   float* dob = qh + s.d_qk;      // [d_v]
@@ -202,24 +202,24 @@ __global__ void __launch_bounds__(128)
   for (int i = 0; i < s.topk; ++i) {
     const int id = ir[i];
     if (id < 0 || id >= s.S_k) continue;
-    float* dr = dkv + (b * s.S_k + id) * s.d_qk;
+    A* dr = dkv + (b * s.S_k + id) * s.d_qk;
     const float gs = s.scale * dS[i], pi = P[i];
     for (int e = threadIdx.x; e < s.d_qk; e += blockDim.x) {
       float v = gs * qh[e];
       if (e < s.d_v) v = fmaf(pi, dob[e], v);
-      atomicAdd(dr + e, v);
+      atomicAdd(dr + e, (A)v);
     }
   }
 }
 
 // [DSA-32K] SparseLightningIndexerGradKLLoss.  grid (rows), block 128.
-template <typename T>
+template <typename T, typename A>
 __global__ void __launch_bounds__(128)
     simt_kl_bwd_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ kv,
                        const T* __restrict__ q_I, const T* __restrict__ k_I,
                        const T* __restrict__ w, const int32_t* __restrict__ idx,
                        const float* __restrict__ mx, const float* __restrict__ sm_in,
-                       float* __restrict__ loss, T* __restrict__ dq_I, float* __restrict__ dk_I,
+                       float* __restrict__ loss, T* __restrict__ dq_I, A* __restrict__ dk_I,
                        float* __restrict__ dw, DevCtx c) {
   extern __shared__ float sh[];
   float* p = sh;                        // [topk]
@@ -291,6 +291,7 @@ __global__ void __launch_bounds__(128)
     for (int i = 0; i < k; ++i) acc = fmaf(p[i], fmaxf(S[j * k + i], 0.f), acc);
     dw[row * s.H_I + j] = acc;
   }
+  __syncthreads();  // dw has read S; it is overwritten in place next
   // dS = dI * w * 1[S > 0]  (in place)
   for (int x = threadIdx.x; x < s.H_I * k; x += blockDim.x) {
     const int j = x / k, i = x % k;
@@ -312,9 +313,18 @@ __global__ void __launch_bounds__(128)
     for (int d = threadIdx.x; d < s.d_I; d += blockDim.x) {
       float acc = 0.f;
       for (int j = 0; j < s.H_I; ++j) acc = fmaf(S[j * k + i], qI[j * s.d_I + d], acc);
-      atomicAdd(dk_I + (b * s.S_k + id) * s.d_I + d, acc);
+      atomicAdd(dk_I + (b * s.S_k + id) * s.d_I + d, (A)acc);
     }
   }
+}
+
+// acc[i] += (float)ws[i]: the exact path accumulates atomics in fp64 and adds
+// the result into the caller's fp32 accumulator once.
+__global__ void add_f64_into_f32(float* __restrict__ acc, const double* __restrict__ ws,
+                                 long long n) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    acc[i] += (float)ws[i];
 }
 
 // ------------------------------- launchers --------------------------------
@@ -371,33 +381,45 @@ int launch_simt_attn_fwd(const Shape& s, bool bf16, const void* q, const void* k
 
 int launch_simt_attn_bwd(const Shape& s, bool bf16, const void* q, const void* kv,
                          const int32_t* idx, const void* out, const void* dout, const float* mx,
-                         const float* sm, void* dq, float* dkv, DevCtx c, cudaStream_t st) {
+                         const float* sm, void* dq, float* dkv, double* ws, DevCtx c,
+                         cudaStream_t st) {
   dim3 g((unsigned)s.H, (unsigned)((long long)s.B * s.S_q));
   const size_t smem = simt_smem_attn_bwd(s);
   if (bf16)
     return launch_big_smem<__nv_bfloat16>(
-        simt_attn_bwd_kernel<__nv_bfloat16>, g, smem, st, s, (const __nv_bfloat16*)q,
+        simt_attn_bwd_kernel<__nv_bfloat16, float>, g, smem, st, s, (const __nv_bfloat16*)q,
         (const __nv_bfloat16*)kv, idx, (const __nv_bfloat16*)out, (const __nv_bfloat16*)dout, mx,
         sm, (__nv_bfloat16*)dq, dkv, c);
-  return launch_big_smem<float>(simt_attn_bwd_kernel<float>, g, smem, st, s, (const float*)q,
-                                (const float*)kv, idx, (const float*)out, (const float*)dout, mx,
-                                sm, (float*)dq, dkv, c);
+  const long long n = (long long)s.B * s.S_k * s.d_qk;
+  if (cudaMemsetAsync(ws, 0, sizeof(double) * n, st) != cudaSuccess) return DSA_ERR_CUDA;
+  int rc = launch_big_smem<float>(simt_attn_bwd_kernel<float, double>, g, smem, st, s,
+                                  (const float*)q, (const float*)kv, idx, (const float*)out,
+                                  (const float*)dout, mx, sm, (float*)dq, ws, c);
+  if (rc) return rc;
+  add_f64_into_f32<<<256, 256, 0, st>>>(dkv, ws, n);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 int launch_simt_kl_bwd(const Shape& s, bool bf16, const void* q, const void* kv, const void* q_I,
                        const void* k_I, const void* w, const int32_t* idx, const float* mx,
-                       const float* sm, float* loss, void* dq_I, float* dk_I, float* dw, DevCtx c,
-                       cudaStream_t st) {
+                       const float* sm, float* loss, void* dq_I, float* dk_I, float* dw,
+                       double* ws, DevCtx c, cudaStream_t st) {
   dim3 g((unsigned)((long long)s.B * s.S_q));
   const size_t smem = simt_smem_kl(s);
   if (bf16)
     return launch_big_smem<__nv_bfloat16>(
-        simt_kl_bwd_kernel<__nv_bfloat16>, g, smem, st, s, (const __nv_bfloat16*)q,
+        simt_kl_bwd_kernel<__nv_bfloat16, float>, g, smem, st, s, (const __nv_bfloat16*)q,
         (const __nv_bfloat16*)kv, (const __nv_bfloat16*)q_I, (const __nv_bfloat16*)k_I,
         (const __nv_bfloat16*)w, idx, mx, sm, loss, (__nv_bfloat16*)dq_I, dk_I, dw, c);
-  return launch_big_smem<float>(simt_kl_bwd_kernel<float>, g, smem, st, s, (const float*)q,
-                                (const float*)kv, (const float*)q_I, (const float*)k_I,
-                                (const float*)w, idx, mx, sm, loss, (float*)dq_I, dk_I, dw, c);
+  const long long n = (long long)s.B * s.S_k * s.d_I;
+  if (cudaMemsetAsync(ws, 0, sizeof(double) * n, st) != cudaSuccess) return DSA_ERR_CUDA;
+  int rc = launch_big_smem<float>(simt_kl_bwd_kernel<float, double>, g, smem, st, s,
+                                  (const float*)q, (const float*)kv, (const float*)q_I,
+                                  (const float*)k_I, (const float*)w, idx, mx, sm, loss,
+                                  (float*)dq_I, ws, dw, c);
+  if (rc) return rc;
+  add_f64_into_f32<<<256, 256, 0, st>>>(dk_I, ws, n);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 }  // namespace dsa

@@ -109,8 +109,9 @@ def test_backward(case):
     idx = torch.as_tensor(ref["idx"], device=DEV)
     dq = torch.empty(1, S, H, d_qk, device=DEV)
     dkv = torch.zeros(1, S, d_qk, device=DEV)
+    ws = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_ATTN_BWD) // 4, device=DEV)
     dsa.sparse_attn_bwd(p, x["q"].to(DEV), x["kv"].to(DEV), idx, f32(ref["O"]), dO.to(DEV),
-                        f32(ref["m"]), f32(ref["l"]), dq, dkv)
+                        f32(ref["m"]), f32(ref["l"]), dq, dkv, ws)
     torch.cuda.synchronize()
     assert np.abs(np64(dq) - dq_r).max() < FP32_TOL
     assert np.abs(np64(dkv) - dkv_r).max() < FP32_TOL
@@ -123,7 +124,8 @@ def test_backward(case):
     dkI = torch.zeros_like(x["k_I"], device=DEV)
     dw = torch.empty_like(x["w"], device=DEV)
     dsa.indexer_kl_loss_bwd(p, x["q"].to(DEV), x["kv"].to(DEV), x["q_I"].to(DEV), x["k_I"].to(DEV),
-                            x["w"].to(DEV), idx, f32(ref["m"]), f32(ref["l"]), loss, dqI, dkI, dw)
+                            x["w"].to(DEV), idx, f32(ref["m"]), f32(ref["l"]), loss, dqI, dkI, dw,
+                            torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_KL_BWD) // 4, device=DEV))
     torch.cuda.synchronize()
     assert abs(float(loss) - loss_r) < FP32_TOL * max(1.0, abs(loss_r))
     assert np.abs(np64(dqI) - dqI_r).max() < FP32_TOL
