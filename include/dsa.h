@@ -191,6 +191,24 @@ int dsa_forward(const dsa_params *p, const void *q_I, const void *k_I, const voi
                 float *softmax_sum, void *workspace, dsa_stream_t stream);
 
 /*
+ * Whole forward with no workspace argument (this library's own addition; the
+ * pages have no counterpart).  For callers that cannot allocate device memory
+ * -- plug-in or custom-operator hosts that pass only input and output
+ * buffers, or latency-critical loops that must not call cudaMalloc or an
+ * allocator -- the score ring lives in a 32 MiB device array inside the
+ * library, held on every GPU that loads the library until the process exits.
+ * Arguments and outputs as dsa_forward; the waves hold as many rows as fit the
+ * ring (a multiple of 4).  The ring's address is looked up on the first call
+ * made on each device (make that call before any stream capture).  All calls
+ * share the ring: calls that overlap on the GPU race on it.
+ * Returns DSA_ERR_UNSUPPORTED when S_k > 2,097,152 (4 score rows would not
+ * fit the ring); never allocates or frees device memory.
+ */
+int dsa_forward_static_ws(const dsa_params *p, const void *q_I, const void *k_I, const void *w,
+                          const void *q, const void *kv, int32_t *idx_out, void *out,
+                          float *softmax_max, float *softmax_sum, dsa_stream_t stream);
+
+/*
  * Device status.  Synchronises `stream`, then writes the device status word
  * of the current device to *device_status (DSA_OK, DSA_ERR_TIMEOUT or
  * DSA_ERR_INDEX) and clears it.  Returns DSA_ERR_CUDA if the stream reported

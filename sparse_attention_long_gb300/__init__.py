@@ -60,6 +60,7 @@ _sigs = {
     "dsa_sparse_attn_bwd": ([_P] + [_vp] * 11, ctypes.c_int),
     "dsa_indexer_kl_loss_bwd": ([_P] + [_vp] * 14, ctypes.c_int),
     "dsa_forward": ([_P] + [_vp] * 11, ctypes.c_int),
+    "dsa_forward_static_ws": ([_P] + [_vp] * 10, ctypes.c_int),
     "dsa_get_status": ([_vp, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
     "dsa_set_wait_budget_ns": ([ctypes.c_uint64], ctypes.c_int),
     "dsa_selftest_wait_timeout": ([ctypes.c_uint64, _vp], ctypes.c_int),
@@ -161,6 +162,14 @@ def forward(p, q_I, k_I, w, q, kv, idx_out, out, softmax_max, softmax_sum, works
     _chk(lib.dsa_forward(ctypes.byref(p), _ptr(q_I), _ptr(k_I), _ptr(w), _ptr(q), _ptr(kv),
                          _ptr(idx_out), _ptr(out), _ptr(softmax_max), _ptr(softmax_sum),
                          _ptr(workspace), _stream(stream)), "dsa_forward")
+
+
+def forward_static_ws(p, q_I, k_I, w, q, kv, idx_out, out, softmax_max, softmax_sum, stream=None):
+    """dsa_forward without a workspace argument: the score ring is the
+    library's own fixed device array (for callers that cannot allocate)."""
+    _chk(lib.dsa_forward_static_ws(ctypes.byref(p), _ptr(q_I), _ptr(k_I), _ptr(w), _ptr(q),
+                                   _ptr(kv), _ptr(idx_out), _ptr(out), _ptr(softmax_max),
+                                   _ptr(softmax_sum), _stream(stream)), "dsa_forward_static_ws")
 
 
 def get_status(stream=None) -> int:

@@ -336,3 +336,23 @@ extern "C" int dsa_selftest_wait_timeout(uint64_t budget_ns, dsa_stream_t stream
   selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(c);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
+
+// Thin non-static entry points into the helpers above, for the scratch-free
+// forward in static_ws.cu (which adds a separate entry point and reuses these
+// unchanged).
+namespace dsa {
+int ext_check_params(const dsa_params* p, Shape* s) { return check_params(p, s); }
+bool ext_dev_ctx(DevCtx* c) { return dev_ctx(c); }
+int ext_attn_fwd_supported(const dsa_params* p, const Shape& s, const void* q, const void* kv) {
+  return attn_fwd_supported(p, s, q, kv);
+}
+int ext_indexer_rows(const dsa_params* p, const Shape& s, const void* q_I, const void* k_I,
+                     const void* w, long long row_begin, long long rows, float* scores,
+                     long long ld, DevCtx c, cudaStream_t st) {
+  return indexer_rows(p, s, q_I, k_I, w, row_begin, rows, scores, ld, false, c, st);
+}
+int ext_attn_fwd(const dsa_params* p, const Shape& s, const void* q, const void* kv,
+                 const int32_t* idx, void* out, float* mx, float* sm, DevCtx c, cudaStream_t st) {
+  return attn_fwd(p, s, q, kv, idx, out, mx, sm, c, st);
+}
+}  // namespace dsa
