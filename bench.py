@@ -354,7 +354,7 @@ def main():
     if world == 1 and not args.no_cpu:
         cpu = cpu_baseline(wl)
     launches_per_step = len(waves) * 2 + 1
-    traffic = kernel_traffic("attn_fwd_tc.cu", "attn_fwd_tc_S32768.md")
+    traffic = kernel_traffic("attn_fwd_tc.cu", "attn_fwd_tc_dsv32.md")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
