@@ -27,7 +27,8 @@
  *    floating tensors fp32 (exact-arithmetic path for small shapes).
  *  - The bf16 path is built for the DeepSeek-V3.2 shapes: H = 128,
  *    d_qk = 576 (512 latent + 64 rope), d_v = 512, H_I = 64, d_I = 128.
- *    Other bf16 shapes return DSA_ERR_UNSUPPORTED.  The fp32 path takes any
+ *    and topk <= 2048 for the attention.  Other bf16 shapes return
+ *    DSA_ERR_UNSUPPORTED.  The fp32 path takes any
  *    H <= 1024, d_qk <= 1024, d_v <= d_qk, H_I <= 256, d_I <= 512,
  *    topk <= 8192.
  *  - Query row t of a CP shard sits at global position

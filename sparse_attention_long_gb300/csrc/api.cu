@@ -143,7 +143,7 @@ static int indexer_rows(const dsa_params* p, const Shape& s, const void* q_I, co
 
 static int attn_fwd_supported(const dsa_params* p, const Shape& s, const void* q, const void* kv) {
   if (p->dtype == DSA_BF16) {
-    if (!tc_attn_shape(p)) return DSA_ERR_UNSUPPORTED;
+    if (!tc_attn_shape(p) || p->topk > 2048) return DSA_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(kv)) return DSA_ERR_INVALID_ARG;
     return DSA_OK;
   }

@@ -10,21 +10,28 @@
 // cluster split the columns: CTA c owns V columns [256c, 256c+256) and rope
 // columns [512+32c, 512+32c+32) -- 288 of the 576 contraction columns and
 // half of O.  Per 64-key block each CTA
-//   1. TMA-gathers (tile::gather4) its 288 columns of the 64 selected kv rows,
-//   2. computes the partial logits S_c = Q_c K_c^T (M=128 heads, N=64, K=288),
-//   3. swaps S_c with its peer through distributed shared memory and forms
-//      S = S_0 + S_1 (the same fp32 sum in both CTAs, so both derive the same
-//      softmax state and the same P without a second exchange),
+//   1. gathers its 288 columns of the 64 selected kv rows into swizzled shared
+//      memory (four producer warps; each warp-wide 16-byte load covers one
+//      key's contiguous 512-byte latent half, so every load is coalesced),
+//   2. computes the partial logits S_c = Q_c K_c^T (M=128 heads, N=64, K=288)
+//      into one of three TMEM logit buffers,
+//   3. swaps S_c with its peer through distributed shared memory (st.async,
+//      completing on the peer's mbarrier) and forms S = S_0 + S_1 (the same
+//      fp32 sum in both CTAs, so both derive the same softmax state and the
+//      same P without a second exchange),
 //   4. runs the fp32 online softmax (one thread per head, exp2 domain; the
-//      running max used for P is only moved when it grows by > 2^8, so the O
-//      rescale in TMEM is rare), writes P as bf16 to shared memory,
-//   5. accumulates O_c += P V_c (M=128, N=256, K=64) in TMEM; V_c is read from
-//      the same gathered tile as an MN-major operand (no second copy).
-// No multiply is duplicated across the pair; the only redundant work is the
-// exp of the shared logits.
+//      running max used for P only moves when it grows by > 2^8, so the O
+//      rescale in TMEM is rare) and writes P as bf16 back over the logits in
+//      TMEM,
+//   5. accumulates O_c += P V_c (M=128, N=256, K=64) with P read from TMEM and
+//      V_c from the same gathered tile as an MN-major operand.
+// No multiply is duplicated across the pair; only the exp of the shared
+// logits is.  The token's index row and per-block validity masks are staged
+// in shared memory once, so no global load sits on the per-block path.
 //
-// Roles per CTA: warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer,
-// warps 2..5 = softmax / exchange / epilogue (thread = head).
+// Roles per CTA: warp 0 = TMEM owner + MMA issuer, warps 1..4 = kv gather (warp 1
+// also TMA-loads the query half), warps 5..12 = softmax / exchange / epilogue:
+// two warps per TMEM lane quadrant, thread = (head, half of the block's keys).
 #include <math.h>
 
 #include "dsa_common.cuh"
@@ -34,19 +41,22 @@ namespace attn {
 
 constexpr int kH = 128, kDQK = 576, kDV = 512;
 constexpr int kBKey = 64;                         // keys per block
-constexpr int kStages = 2;
+constexpr int kMaxTopk = 2048;                    // index row staged in shared memory
+constexpr int kMaxBlk = kMaxTopk / kBKey;
+constexpr int kStages = 3;                        // KV gather stages
+constexpr int kSBuf = 3;                          // TMEM logit / P buffers
 constexpr int kQChunk = kH * 128;                 // 64 cols x 128 heads (SW128)
 constexpr int kQRope = kH * 64;                   // 32 cols x 128 heads (SW64)
 constexpr int kQBytes = 4 * kQChunk + kQRope;     // 72 KB
 constexpr int kKVChunk = kBKey * 128;             // 8 KB
 constexpr int kKVRope = kBKey * 64;               // 4 KB
 constexpr int kKVStage = 4 * kKVChunk + kKVRope;  // 36 KB
-constexpr int kPBytes = kH * 128;                 // 128 heads x 64 keys bf16
-constexpr int kXBytes = kH * kBKey * 4;           // 32 KB fp32 partial logits
-constexpr int kSoftWarps = 4;
-constexpr int kThreads = 64 + kSoftWarps * 32;
+constexpr int kSoftWarps = 8;                     // two per TMEM lane quadrant
+constexpr int kGatherWarps = 4;
+constexpr int kWarpMMA = 0, kWarpGather0 = 1, kWarpSoft0 = kWarpGather0 + kGatherWarps;
+constexpr int kThreads = 32 * (1 + kGatherWarps + kSoftWarps);
 constexpr int kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 256;
+constexpr uint32_t kColO = 0, kColS = 256;        // O: [0,256)  logits/P: 256 + 64*b
 constexpr uint32_t kIdescS = idesc_bf16(128, kBKey, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
@@ -56,14 +66,18 @@ constexpr float kLn2 = 0.6931471805599453f;
 struct __align__(1024) Smem {
   uint8_t q[kQBytes];
   uint8_t kv[kStages][kKVStage];
-  uint8_t p[2][kPBytes];
-  float x[kH * kBKey];
-  uint64_t q_full, kv_full[kStages], kv_empty[kStages], s_full[2], s_empty[2], p_full[2],
-      p_empty[2], pv_done, x_full, x_free, mma_done;
+  float x[kH * kBKey];                            // peer's partial logits [16 x 4-key chunk][head][4]
+  float red[2][2][kH];                            // per-block max of each key half (double buffered)
+  int32_t idx[kMaxTopk];                          // the token's index row (-1 = skip)
+  unsigned long long mask[kMaxBlk];               // per 64-slot block: valid slots
+  uint64_t q_full, kv_full[kStages], kv_empty[kStages], s_full[kSBuf], s_free[kSBuf],
+      p_full[kSBuf], pv_done, x_full, x_free, mma_done;
   uint32_t tmem_base;
   int abort;
-  int nblk;
+  int last;
+  int bad;
 };
+static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory budget");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -71,10 +85,20 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qr,
-                       const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kvr,
-                       Shape s, const int32_t* __restrict__ idx, __nv_bfloat16* __restrict__ out,
+                       const void* __restrict__ kvg, Shape s, const int32_t* __restrict__ idx,
+                       __nv_bfloat16* __restrict__ out,
                        float* __restrict__ mx, float* __restrict__ sm_out, long long nrows,
                        DevCtx c) {
   extern __shared__ uint8_t smem_raw[];
@@ -87,111 +111,124 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int k = s.topk;
   const int32_t* irow = idx + row * (long long)k;
   volatile int* abort_flag = &sm.abort;
+  const uint32_t q0 = smem_u32(sm.q);
 
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 32 * kWarpGather0) {
     mbar_init(smem_u32(&sm.q_full), 1);
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(smem_u32(&sm.kv_full[i]), 1);
+      mbar_init(smem_u32(&sm.kv_full[i]), kGatherWarps * 32);
       mbar_init(smem_u32(&sm.kv_empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBuf; ++i) {
       mbar_init(smem_u32(&sm.s_full[i]), 1);
-      mbar_init(smem_u32(&sm.s_empty[i]), kSoftWarps * 32);
+      mbar_init(smem_u32(&sm.s_free[i]), 1);
       mbar_init(smem_u32(&sm.p_full[i]), kSoftWarps * 32);
-      mbar_init(smem_u32(&sm.p_empty[i]), 1);
     }
     mbar_init(smem_u32(&sm.pv_done), 1);
-    mbar_init(smem_u32(&sm.x_full), kSoftWarps * 32);  // arrivals come from the peer
-    mbar_init(smem_u32(&sm.x_free), kSoftWarps * 32);  // arrivals come from the peer
+    mbar_init(smem_u32(&sm.x_full), 1);            // local arm + the peer's st.async bytes
+    mbar_init(smem_u32(&sm.x_free), kSoftWarps);   // one arrive per peer softmax warp
     mbar_init(smem_u32(&sm.mma_done), 1);
     sm.abort = 0;
+    sm.last = -1;
+    sm.bad = 0;
     fence_mbar_init();
+    // the token's query half is independent of everything else: start it now
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_qr);
+    const uint32_t qb = smem_u32(&sm.q_full);
+    mbar_arrive_expect_tx(qb, kQBytes);
+    const int qrow = (int)(row * kH);
+    for (int i = 0; i < 4; ++i)
+      tma_load_2d(q0 + i * kQChunk, &tm_q, (int)(256 * crank + 64 * i), qrow, qb);
+    tma_load_2d(q0 + 4 * kQChunk, &tm_qr, (int)(512 + 32 * crank), qrow, qb);
   }
-  if (warp == 0) {
-    // number of 64-slot blocks up to the last valid index of this row
-    int last = -1;
-    for (int i = lane; i < k; i += 32) {
-      const int id = irow[i];
-      if (id >= 0 && id < s.S_k) last = i;
-      else if (id < -1 || id >= s.S_k) set_status(c, DSA_ERR_INDEX);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-    if (lane == 0) sm.nblk = (last + kBKey) / kBKey;
-  }
-  if (warp == 1) {
+  if (warp == kWarpMMA) {
     tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
     tmem_relinquish();
     tc_fence_before();
   }
+  // stage the index row: out-of-range entries become -1 (skipped, reported)
+  int last = -1, bad = 0;
+  for (int i = threadIdx.x; i < k; i += kThreads) {
+    int id = irow[i];
+    if (id < -1 || id >= s.S_k) bad = 1;
+    if (id < 0 || id >= s.S_k) id = -1;
+    else last = i;
+    sm.idx[i] = id;
+  }
+  __syncthreads();  // barrier init (sm.last / sm.bad) and the staged row are visible
+  if (last >= 0) atomicMax(&sm.last, last);
+  if (bad) sm.bad = 1;
+  __syncthreads();
+  const int nblk = (sm.last + kBKey) / kBKey;
+  for (int j = warp; j < nblk; j += kThreads / 32) {
+    const int s0 = j * kBKey + lane, s1 = s0 + 32;
+    const uint32_t lo = __ballot_sync(0xffffffffu, s0 < k && sm.idx[s0] >= 0);
+    const uint32_t hi = __ballot_sync(0xffffffffu, s1 < k && sm.idx[s1] >= 0);
+    if (lane == 0) sm.mask[j] = ((unsigned long long)hi << 32) | lo;
+  }
+  if (threadIdx.x == 0 && sm.bad) set_status(c, DSA_ERR_INDEX);
   __syncthreads();
   cluster_sync_all();  // both CTAs' barriers initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  const int nblk = sm.nblk;
-  const uint32_t q0 = smem_u32(sm.q);
 
-  if (warp == 0) {
-    // ------------------------------ TMA producer ------------------------------
-    if (nblk > 0) {
-      if (lane == 0) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_qr);
-        tma_prefetch_desc(&tm_kv);
-        tma_prefetch_desc(&tm_kvr);
-        const uint32_t qb = smem_u32(&sm.q_full);
-        mbar_arrive_expect_tx(qb, kQBytes);
-        const int qrow = (int)(row * kH);
-        for (int i = 0; i < 4; ++i)
-          tma_load_2d(q0 + i * kQChunk, &tm_q, (int)(256 * crank + 64 * i), qrow, qb);
-        tma_load_2d(q0 + 4 * kQChunk, &tm_qr, (int)(512 + 32 * crank), qrow, qb);
-      }
-      const int kvbase = (int)(b * s.S_k);
-      int j = 0;
-      for (; j < nblk; ++j) {
-        const int st = j % kStages;
-        if (!mbar_wait_warp(smem_u32(&sm.kv_empty[st]), ((j / kStages) & 1) ^ 1, c, abort_flag)) break;
-        // this block's 64 rows: lane holds slots lane and lane+32 (invalid -> row 0)
-        const int s0 = j * kBKey + lane, s1 = s0 + 32;
-        int i0 = s0 < k ? irow[s0] : -1;
-        int i1 = s1 < k ? irow[s1] : -1;
-        i0 = (i0 >= 0 && i0 < s.S_k) ? kvbase + i0 : kvbase;
-        i1 = (i1 >= 0 && i1 < s.S_k) ? kvbase + i1 : kvbase;
-        const uint32_t fb = smem_u32(&sm.kv_full[st]);
-        const uint32_t dst = smem_u32(sm.kv[st]);
-        if (lane == 0) mbar_arrive_expect_tx(fb, kKVStage);
-#pragma unroll 1
-        for (int g = 0; g < kBKey / 4; ++g) {
-          const int src_lane = (g * 4) & 31;
-          const int v0 = __shfl_sync(0xffffffffu, g < 8 ? i0 : i1, src_lane + 0);
-          const int v1 = __shfl_sync(0xffffffffu, g < 8 ? i0 : i1, src_lane + 1);
-          const int v2 = __shfl_sync(0xffffffffu, g < 8 ? i0 : i1, src_lane + 2);
-          const int v3 = __shfl_sync(0xffffffffu, g < 8 ? i0 : i1, src_lane + 3);
-          if (lane == 0) {
+  if (warp >= kWarpGather0 && warp < kWarpSoft0) {
+    // ------------------------------- kv gather -------------------------------
+    // warp gw owns keys gw, gw+4, ..., gw+60 of every block.  Latent half: one
+    // warp-wide 16-byte load per key (lane = 16-byte chunk of the 512 bytes);
+    // rope quarter: 8 keys x 4 chunks per load.  Stores follow the SW128 (latent,
+    // 64 columns per 128-byte row) and SW64 (rope, 32 columns) K-major layouts.
+    const int gw = warp - kWarpGather0;
+    const __nv_bfloat16* kvb = reinterpret_cast<const __nv_bfloat16*>(kvg) + b * s.S_k * (long long)kDQK;
+    const int lat_col = 256 * (int)crank + 8 * lane;               // this lane's latent chunk
+    const int rope_m = lane >> 2, rope_c = lane & 3;
+    const int rope_col = 512 + 32 * (int)crank + 8 * rope_c;
+    for (int j = 0; j < nblk; ++j) {
+      const int st = j % kStages;
+      if (!mbar_wait_warp(smem_u32(&sm.kv_empty[st]), ((j / kStages) & 1) ^ 1, c, abort_flag)) break;
+      uint4 lat[16], rope[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              tma_gather4(dst + i * kKVChunk + g * 512, &tm_kv, (int)(256 * crank + 64 * i), v0, v1,
-                          v2, v3, fb);
-            tma_gather4(dst + 4 * kKVChunk + g * 256, &tm_kvr, (int)(512 + 32 * crank), v0, v1, v2,
-                        v3, fb);
-          }
-        }
+      for (int m = 0; m < 16; ++m) {
+        const int e = j * kBKey + gw + 4 * m;
+        const int id = e < k ? sm.idx[e] : -1;
+        lat[m] = __ldg(reinterpret_cast<const uint4*>(kvb + (long long)(id < 0 ? 0 : id) * kDQK + lat_col));
       }
-      if (lane == 0) {  // drain: every issued copy has landed before exit
-        mbar_wait(smem_u32(&sm.q_full), 0, c, abort_flag);
-        for (int i = (j > kStages ? j - kStages : 0); i < j; ++i)
-          mbar_wait(smem_u32(&sm.kv_full[i % kStages]), (i / kStages) & 1, c, abort_flag);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int e = j * kBKey + gw + 4 * (8 * i + rope_m);
+        const int id = e < k ? sm.idx[e] : -1;
+        rope[i] = __ldg(reinterpret_cast<const uint4*>(kvb + (long long)(id < 0 ? 0 : id) * kDQK + rope_col));
       }
+      const uint32_t kvs = smem_u32(sm.kv[st]);
+      const int g = lane >> 3, cc = lane & 7;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const int r = gw + 4 * m;
+        const uint32_t dst = kvs + g * kKVChunk + r * 128 + ((cc ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(lat[m].x),
+                     "r"(lat[m].y), "r"(lat[m].z), "r"(lat[m].w) : "memory");
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int r = gw + 4 * (8 * i + rope_m);
+        const uint32_t dst = kvs + 4 * kKVChunk + r * 64 + ((rope_c ^ ((r >> 1) & 3)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(rope[i].x),
+                     "r"(rope[i].y), "r"(rope[i].z), "r"(rope[i].w) : "memory");
+      }
+      fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor cores
+      mbar_arrive(smem_u32(&sm.kv_full[st]));
     }
-  } else if (warp == 1) {
+    if (warp == kWarpGather0 && lane == 0) mbar_wait(smem_u32(&sm.q_full), 0, c, abort_flag);
+  } else if (warp == kWarpMMA) {
     // ------------------------------- MMA issuer -------------------------------
     if (lane == 0 && nblk > 0) {
       bool ok = mbar_wait(smem_u32(&sm.q_full), 0, c, abort_flag);
       for (int step = 0; ok && step <= nblk; ++step) {
-        if (step < nblk) {  // S(step) = Q_c K_c^T
-          const int j = step, st = j % kStages, sb = j & 1;
+        if (step < nblk) {  // S(step) = Q_c K_c^T into logit buffer step % 3
+          const int j = step, st = j % kStages, sb = j % kSBuf;
           if (!mbar_wait(smem_u32(&sm.kv_full[st]), (j / kStages) & 1, c, abort_flag)) break;
-          if (!mbar_wait(smem_u32(&sm.s_empty[sb]), ((j >> 1) & 1) ^ 1, c, abort_flag)) break;
+          if (!mbar_wait(smem_u32(&sm.s_free[sb]), ((j / kSBuf) & 1) ^ 1, c, abort_flag)) break;
           tc_fence_after();
           const uint32_t kv0 = smem_u32(sm.kv[st]);
           const uint32_t d = tmem + kColS + sb * kBKey;
@@ -210,20 +247,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           mma_commit(smem_u32(&sm.s_full[sb]));
         }
-        if (step >= 1) {  // O_c += P V_c for block step-1
-          const int j = step - 1, st = j % kStages, pb = j & 1;
-          if (!mbar_wait(smem_u32(&sm.p_full[pb]), (j >> 1) & 1, c, abort_flag)) break;
+        if (step >= 1) {  // O_c += P V_c for block step-1 (P in TMEM over its logits)
+          const int j = step - 1, st = j % kStages, sb = j % kSBuf;
+          if (!mbar_wait(smem_u32(&sm.p_full[sb]), (j / kSBuf) & 1, c, abort_flag)) break;
           tc_fence_after();
           const uint32_t kv0 = smem_u32(sm.kv[st]);
-          const uint32_t p0 = smem_u32(sm.p[pb]);
+          const uint32_t pa = tmem + kColS + sb * kBKey;
 #pragma unroll
           for (int kk = 0; kk < kBKey / 16; ++kk) {
-            const uint64_t ad = sdesc(p0 + kk * 32, 16, 1024, kSw128);
             const uint64_t bd = sdesc(kv0 + kk * 2048, kKVChunk, 1024, kSw128);
-            mma_bf16_ss(tmem + kColO, ad, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_ts(tmem + kColO, pa + kk * 8, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(smem_u32(&sm.kv_empty[st]));
-          mma_commit(smem_u32(&sm.p_empty[pb]));
+          mma_commit(smem_u32(&sm.s_free[sb]));
           mma_commit(smem_u32(&sm.pv_done));
         }
       }
@@ -232,69 +268,80 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else {
     // ----------------------- softmax / exchange / epilogue --------------------
+    const int sw = warp - kWarpSoft0;                    // 0..7
+    const int hf = sw >> 2;                              // key half of each block
     const int quad = warp & 3;
     const int h = quad * 32 + lane;                      // this thread's head (TMEM lane)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t x_local = smem_u32(sm.x) + h * 256;
-    const uint32_t x_remote = mapa_shared(x_local, peer);
-    const uint32_t xfull_remote = mapa_shared(smem_u32(&sm.x_full), peer);
+    const uint32_t xfull = smem_u32(&sm.x_full);
+    const uint32_t x_remote = mapa_shared(smem_u32(sm.x), peer);
+    const uint32_t xfull_remote = mapa_shared(xfull, peer);
     const uint32_t xfree_remote = mapa_shared(smem_u32(&sm.x_free), peer);
     const float sl2e = s.scale * kLog2e;
-    float m_run = -INFINITY, m_true = -INFINITY, l_run = 0.f, lr_run = 0.f;
+    const bool armer = (sw == 0 && lane == 0);
+    float m_run = -INFINITY, m_true = -INFINITY, l_run = 0.f;
+    // A failed (timed-out) wait turns the rest of this warp's work into no-ops,
+    // but every softmax warp still executes the same named barriers.
     bool ok = true;
-    for (int j = 0; ok && j < nblk; ++j) {
-      const int sb = j & 1;
-      const int s0 = j * kBKey + lane, s1 = s0 + 32;
-      const int i0 = s0 < k ? irow[s0] : -1, i1 = s1 < k ? irow[s1] : -1;
-      const uint32_t mlo = __ballot_sync(0xffffffffu, i0 >= 0 && i0 < s.S_k);
-      const uint32_t mhi = __ballot_sync(0xffffffffu, i1 >= 0 && i1 < s.S_k);
-      if (!mbar_wait_warp(smem_u32(&sm.s_full[sb]), (j >> 1) & 1, c, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t u[2][32];
-      tmem_ld32(tmem + lane_off + kColS + sb * kBKey, u[0]);
-      tmem_ld32(tmem + lane_off + kColS + sb * kBKey + 32, u[1]);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.s_empty[sb]));
-      // send my partial logits to the peer (row h, 16-byte chunks swizzled by h)
-      if (!mbar_wait_warp<true>(smem_u32(&sm.x_free), (j & 1) ^ 1, c, abort_flag)) { ok = false; break; }
-#pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        const uint32_t* src = &u[ch >> 3][(ch & 7) * 4];
-        st_cluster_v4(x_remote + ((ch ^ (h & 15)) << 4), __uint_as_float(src[0]),
-                      __uint_as_float(src[1]), __uint_as_float(src[2]), __uint_as_float(src[3]));
+    for (int j = 0; j < nblk; ++j) {
+      const int sb = j % kSBuf;
+      const uint32_t vmask = (uint32_t)(sm.mask[j] >> (32 * hf));
+      const uint32_t sbuf = tmem + lane_off + kColS + sb * kBKey;
+      if (ok && armer) mbar_arrive_expect_tx(xfull, kH * kBKey * 4);  // phase j of x_full
+      ok = ok && mbar_wait_warp(smem_u32(&sm.s_full[sb]), (j / kSBuf) & 1, c, abort_flag);
+      uint32_t u[32];
+      if (ok) {
+        tc_fence_after();
+        tmem_ld32(sbuf + 32 * hf, u);
+        tmem_ld_wait();
       }
-      mbar_arrive_remote(xfull_remote);
-      if (!mbar_wait_warp<true>(smem_u32(&sm.x_full), j & 1, c, abort_flag)) { ok = false; break; }
-      float v[64];
+      // my partial logits -> the peer's exchange buffer, completing on its x_full
+      ok = ok && mbar_wait_warp<true>(smem_u32(&sm.x_free), (j & 1) ^ 1, c, abort_flag);
+      if (ok) {
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        const float4 pr = *reinterpret_cast<const float4*>(sm.x + h * 64 + ((ch ^ (h & 15)) << 2));
-        const uint32_t* own = &u[ch >> 3][(ch & 7) * 4];
-        v[ch * 4 + 0] = __uint_as_float(own[0]) + pr.x;
-        v[ch * 4 + 1] = __uint_as_float(own[1]) + pr.y;
-        v[ch * 4 + 2] = __uint_as_float(own[2]) + pr.z;
-        v[ch * 4 + 3] = __uint_as_float(own[3]) + pr.w;
+        for (int ch = 0; ch < 8; ++ch)
+          st_async_v4(x_remote + (((8 * hf + ch) * kH + h) << 4), u[4 * ch], u[4 * ch + 1],
+                      u[4 * ch + 2], u[4 * ch + 3], xfull_remote);
       }
-      mbar_arrive_remote(xfree_remote);
+      ok = ok && mbar_wait_warp<true>(xfull, j & 1, c, abort_flag);
+      float v[32];
       float bm = -INFINITY;
+      if (ok) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const bool valid = ((i < 32 ? mlo >> i : mhi >> (i - 32)) & 1u) != 0;
-        v[i] = valid ? v[i] * sl2e : -INFINITY;
-        bm = fmaxf(bm, v[i]);
+        for (int ch = 0; ch < 8; ++ch) {
+          const float4 pr = *reinterpret_cast<const float4*>(sm.x + ((8 * hf + ch) * kH + h) * 4);
+          v[4 * ch + 0] = __uint_as_float(u[4 * ch + 0]) + pr.x;
+          v[4 * ch + 1] = __uint_as_float(u[4 * ch + 1]) + pr.y;
+          v[4 * ch + 2] = __uint_as_float(u[4 * ch + 2]) + pr.z;
+          v[4 * ch + 3] = __uint_as_float(u[4 * ch + 3]) + pr.w;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(xfree_remote);  // the values are in registers
+        if (vmask != 0xffffffffu) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (((vmask >> i) & 1u) == 0) v[i] = -INFINITY;
+        }
+        bm = v[0];
+#pragma unroll
+        for (int i = 1; i < 32; ++i) bm = fmaxf(bm, v[i]);
       }
+      sm.red[j & 1][hf][h] = bm;
+      named_bar_sync(1, kSoftWarps * 32);  // both halves loaded their logits; maxima visible
+      if (!ok) continue;
+      bm = fmaxf(bm, sm.red[j & 1][hf ^ 1][h]) * sl2e;  // block max, log2 units (sl2e > 0)
       m_true = fmaxf(m_true, bm);
       const bool need = bm > m_run + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need)) {
+      if (__any_sync(0xffffffffu, need)) {  // same vote in both halves (same maxima)
         const float m_new = fmaxf(m_run, bm);
         const float alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - m_new);
         if (j > 0 && __any_sync(0xffffffffu, m_run != -INFINITY)) {
-          // O must hold PV(j-1) before it is rescaled
-          if (!mbar_wait_warp(smem_u32(&sm.pv_done), (j - 1) & 1, c, abort_flag)) { ok = false; break; }
+          // O must hold PV(j-1) before it is rescaled; each half owns 128 columns
+          ok = mbar_wait_warp(smem_u32(&sm.pv_done), (j - 1) & 1, c, abort_flag);
+          if (!ok) continue;
           tc_fence_after();
 #pragma unroll 1
-          for (int cc = 0; cc < 256; cc += 32) {
+          for (int cc = 128 * hf; cc < 128 * hf + 128; cc += 32) {
             uint32_t o[32];
             tmem_ld32(tmem + lane_off + kColO + cc, o);
             tmem_ld_wait();
@@ -302,32 +349,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
             tmem_st32(tmem + lane_off + kColO + cc, o);
           }
-          tmem_st_wait();
         }
         l_run *= alpha;
-        lr_run *= alpha;
         m_run = m_new;
       }
       const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-      if (!mbar_wait_warp(smem_u32(&sm.p_empty[sb]), ((j >> 1) & 1) ^ 1, c, abort_flag)) { ok = false; break; }
-      const uint32_t prow = smem_u32(sm.p[sb]) + h * 128;
+      uint32_t pk[16];
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float pa = ex2(v[ch * 8 + 2 * q] - mu);
-          const float pb = ex2(v[ch * 8 + 2 * q + 1] - mu);
-          l_run += pa + pb;
-          pk[q] = pack_bf16x2(pa, pb);
-          __nv_bfloat162 r = *reinterpret_cast<__nv_bfloat162*>(&pk[q]);
-          lr_run += __low2float(r) + __high2float(r);
-        }
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((ch ^ (h & 7)) << 4)),
-                     "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
-                     : "memory");
+      for (int i = 0; i < 16; ++i) {
+        const float pa = ex2(fmaf(v[2 * i], sl2e, -mu));
+        const float pb = ex2(fmaf(v[2 * i + 1], sl2e, -mu));
+        l_run += pa + pb;
+        pk[i] = pack_bf16x2(pa, pb);
       }
-      fence_proxy_async_smem();
+      tmem_st16(sbuf + 16 * hf, pk);  // P (bf16 pairs) over the logits of this block
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.p_full[sb]));
     }
@@ -335,13 +371,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool have = ok && nblk > 0;
     if (have) have = mbar_wait_warp(smem_u32(&sm.pv_done), (nblk - 1) & 1, c, abort_flag);
     tc_fence_after();
-    const float inv = (have && lr_run > 0.f) ? 1.f / lr_run : 0.f;
-    __nv_bfloat16* orow = out + (row * kH + h) * (long long)kDV + 256 * crank;
+    sm.red[nblk & 1][hf][h] = l_run;  // the buffer the last block's maxima did not use
+    named_bar_sync(1, kSoftWarps * 32);
+    const float l_all = sm.red[nblk & 1][0][h] + sm.red[nblk & 1][1][h];
+    const float inv = (have && l_all > 0.f) ? 1.f / l_all : 0.f;
+    const int c0 = 128 * hf;
+    __nv_bfloat16* orow = out + (row * kH + h) * (long long)kDV + 256 * crank + c0;
 #pragma unroll 1
-    for (int cc = 0; cc < 256; cc += 32) {
+    for (int cc = 0; cc < 128; cc += 32) {
       uint32_t o[32];
       if (__all_sync(0xffffffffu, have)) {
-        tmem_ld32(tmem + lane_off + kColO + cc, o);
+        tmem_ld32(tmem + lane_off + kColO + c0 + cc, o);
         tmem_ld_wait();
       } else {
 #pragma unroll
@@ -356,16 +396,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 4; ++i) dst[i] = pk[i];
     }
-    if (crank == 0) {
+    if (crank == 0 && hf == 0) {
       const bool any = have && m_true != -INFINITY;
       mx[row * kH + h] = any ? m_true * kLn2 : -INFINITY;
-      sm_out[row * kH + h] = any ? l_run * ex2(m_run - m_true) : 0.f;
+      sm_out[row * kH + h] = any ? l_all * ex2(m_run - m_true) : 0.f;
     }
   }
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // the peer may still be arriving on our barriers until here
-  if (warp == 1) {
+  if (warp == kWarpMMA) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -376,22 +416,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 bool make_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
                        uint32_t box_cols, uint32_t box_rows, int swizzle_bytes);
 
+int attn_fwd_tc_max_topk() { return attn::kMaxTopk; }
+
 int launch_attn_fwd_tc(const Shape& s, const void* q, const void* kv, const int32_t* idx, void* out,
                        float* mx, float* sm, DevCtx c, cudaStream_t st) {
   using namespace attn;
-  CUtensorMap tq, tqr, tkv, tkvr;
-  const uint64_t qrows = (uint64_t)s.B * s.S_q * kH, kvrows = (uint64_t)s.B * s.S_k;
+  if (s.topk > kMaxTopk) return DSA_ERR_UNSUPPORTED;
+  CUtensorMap tq, tqr;
+  const uint64_t qrows = (uint64_t)s.B * s.S_q * kH;
   if (!make_tmap_2d_bf16(&tq, q, qrows, kDQK, 64, kH, 128)) return DSA_ERR_CUDA;
   if (!make_tmap_2d_bf16(&tqr, q, qrows, kDQK, 32, kH, 64)) return DSA_ERR_CUDA;
-  if (!make_tmap_2d_bf16(&tkv, kv, kvrows, kDQK, 64, 1, 128)) return DSA_ERR_CUDA;
-  if (!make_tmap_2d_bf16(&tkvr, kv, kvrows, kDQK, 32, 1, 64)) return DSA_ERR_CUDA;
   const size_t smem = sizeof(Smem) + 1024;
   if (cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return DSA_ERR_CUDA;
   const long long nrows = (long long)s.B * s.S_q;
   attn_fwd_tc_kernel<<<(unsigned)(2 * nrows), kThreads, smem, st>>>(
-      tq, tqr, tkv, tkvr, s, idx, (__nv_bfloat16*)out, mx, sm, nrows, c);
+      tq, tqr, kv, s, idx, (__nv_bfloat16*)out, mx, sm, nrows, c);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
