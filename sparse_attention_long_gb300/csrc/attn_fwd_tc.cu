@@ -71,7 +71,7 @@ struct __align__(1024) Smem {
   int32_t idx[kMaxTopk];                          // the token's index row (-1 = skip)
   unsigned long long mask[kMaxBlk];               // per 64-slot block: valid slots
   uint64_t q_full, kv_full[kStages], kv_empty[kStages], s_full[kSBuf], s_free[kSBuf],
-      p_full[kSBuf], pv_done, x_full, x_free, mma_done;
+      p_full[kSBuf], x_full, x_free, mma_done;
   uint32_t tmem_base;
   int abort;
   int last;
@@ -124,7 +124,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm.s_free[i]), 1);
       mbar_init(smem_u32(&sm.p_full[i]), kSoftWarps * 32);
     }
-    mbar_init(smem_u32(&sm.pv_done), 1);
     mbar_init(smem_u32(&sm.x_full), 1);            // local arm + the peer's st.async bytes
     mbar_init(smem_u32(&sm.x_free), kSoftWarps);   // one arrive per peer softmax warp
     mbar_init(smem_u32(&sm.mma_done), 1);
@@ -223,44 +222,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMMA) {
     // ------------------------------- MMA issuer -------------------------------
     if (lane == 0 && nblk > 0) {
+      // Issue whichever is ready: the logits S(ns) of the next block (needs its
+      // gathered tile and a free logit buffer, i.e. PV(ns-3) done) or PV(np) of
+      // the oldest block whose P is written.  S runs at most one block ahead of
+      // the PVs issued so far (letting it run two ahead produced rare
+      // run-to-run differences in a few rows; see the design notes).
       bool ok = mbar_wait(smem_u32(&sm.q_full), 0, c, abort_flag);
-      for (int step = 0; ok && step <= nblk; ++step) {
-        if (step < nblk) {  // S(step) = Q_c K_c^T into logit buffer step % 3
-          const int j = step, st = j % kStages, sb = j % kSBuf;
-          if (!mbar_wait(smem_u32(&sm.kv_full[st]), (j / kStages) & 1, c, abort_flag)) break;
-          if (!mbar_wait(smem_u32(&sm.s_free[sb]), ((j / kSBuf) & 1) ^ 1, c, abort_flag)) break;
-          tc_fence_after();
-          const uint32_t kv0 = smem_u32(sm.kv[st]);
-          const uint32_t d = tmem + kColS + sb * kBKey;
+      int ns = 0, np = 0;
+      uint64_t t_idle = 0;
+      uint32_t spins = 0;
+      while (ok && np < nblk) {
+        bool progressed = false;
+        if (ns < nblk && ns < np + 2) {
+          const int st = ns % kStages, sb = ns % kSBuf;
+          if (mbar_test(smem_u32(&sm.kv_full[st]), (ns / kStages) & 1) &&
+              mbar_test(smem_u32(&sm.s_free[sb]), ((ns / kSBuf) & 1) ^ 1)) {
+            tc_fence_after();
+            const uint32_t kv0 = smem_u32(sm.kv[st]);
+            const uint32_t d = tmem + kColS + sb * kBKey;
 #pragma unroll
-          for (int kk = 0; kk < 16; ++kk) {
-            const uint32_t off = (kk & 3) * 32;
-            const uint64_t ad = sdesc(q0 + (kk >> 2) * kQChunk + off, 16, 1024, kSw128);
-            const uint64_t bd = sdesc(kv0 + (kk >> 2) * kKVChunk + off, 16, 1024, kSw128);
-            mma_bf16_ss(d, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
-          }
+            for (int kk = 0; kk < 16; ++kk) {
+              const uint32_t off = (kk & 3) * 32;
+              const uint64_t ad = sdesc(q0 + (kk >> 2) * kQChunk + off, 16, 1024, kSw128);
+              const uint64_t bd = sdesc(kv0 + (kk >> 2) * kKVChunk + off, 16, 1024, kSw128);
+              mma_bf16_ss(d, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+            }
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const uint64_t ad = sdesc(q0 + 4 * kQChunk + kk * 32, 16, 512, kSw64);
-            const uint64_t bd = sdesc(kv0 + 4 * kKVChunk + kk * 32, 16, 512, kSw64);
-            mma_bf16_ss(d, ad, bd, kIdescS, 1u);
+            for (int kk = 0; kk < 2; ++kk) {
+              const uint64_t ad = sdesc(q0 + 4 * kQChunk + kk * 32, 16, 512, kSw64);
+              const uint64_t bd = sdesc(kv0 + 4 * kKVChunk + kk * 32, 16, 512, kSw64);
+              mma_bf16_ss(d, ad, bd, kIdescS, 1u);
+            }
+            mma_commit(smem_u32(&sm.s_full[sb]));
+            ++ns;
+            progressed = true;
           }
-          mma_commit(smem_u32(&sm.s_full[sb]));
         }
-        if (step >= 1) {  // O_c += P V_c for block step-1 (P in TMEM over its logits)
-          const int j = step - 1, st = j % kStages, sb = j % kSBuf;
-          if (!mbar_wait(smem_u32(&sm.p_full[sb]), (j / kSBuf) & 1, c, abort_flag)) break;
-          tc_fence_after();
-          const uint32_t kv0 = smem_u32(sm.kv[st]);
-          const uint32_t pa = tmem + kColS + sb * kBKey;
+        if (np < ns) {
+          const int st = np % kStages, sb = np % kSBuf;
+          if (mbar_test(smem_u32(&sm.p_full[sb]), (np / kSBuf) & 1)) {
+            tc_fence_after();
+            const uint32_t kv0 = smem_u32(sm.kv[st]);
+            const uint32_t pa = tmem + kColS + sb * kBKey;
 #pragma unroll
-          for (int kk = 0; kk < kBKey / 16; ++kk) {
-            const uint64_t bd = sdesc(kv0 + kk * 2048, kKVChunk, 1024, kSw128);
-            mma_bf16_ts(tmem + kColO, pa + kk * 8, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBKey / 16; ++kk) {
+              const uint64_t bd = sdesc(kv0 + kk * 2048, kKVChunk, 1024, kSw128);
+              mma_bf16_ts(tmem + kColO, pa + kk * 8, bd, kIdescPV, (np > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(smem_u32(&sm.kv_empty[st]));
+            mma_commit(smem_u32(&sm.s_free[sb]));
+            ++np;
+            progressed = true;
           }
-          mma_commit(smem_u32(&sm.kv_empty[st]));
-          mma_commit(smem_u32(&sm.s_free[sb]));
-          mma_commit(smem_u32(&sm.pv_done));
+        }
+        if (progressed) {
+          spins = 0;
+        } else if ((++spins & 63u) == 0) {  // bounded: no progress for the wait budget
+          const uint64_t now = globaltimer();
+          if (t_idle == 0 || spins == 64) t_idle = now;
+          if (*abort_flag) ok = false;
+          else if (now - t_idle > c.budget) {
+            set_status(c, DSA_ERR_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+          }
         }
       }
       mma_commit(smem_u32(&sm.mma_done));
@@ -280,32 +305,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float sl2e = s.scale * kLog2e;
     const bool armer = (sw == 0 && lane == 0);
     float m_run = -INFINITY, m_true = -INFINITY, l_run = 0.f;
+    // Software-pipelined: block j+1's partial logits go out to the peer before
+    // block j's softmax arithmetic, so the exchange latency overlaps it.
     // A failed (timed-out) wait turns the rest of this warp's work into no-ops,
     // but every softmax warp still executes the same named barriers.
     bool ok = true;
-    for (int j = 0; j < nblk; ++j) {
-      const int sb = j % kSBuf;
-      const uint32_t vmask = (uint32_t)(sm.mask[j] >> (32 * hf));
-      const uint32_t sbuf = tmem + lane_off + kColS + sb * kBKey;
-      if (ok && armer) mbar_arrive_expect_tx(xfull, kH * kBKey * 4);  // phase j of x_full
-      ok = ok && mbar_wait_warp(smem_u32(&sm.s_full[sb]), (j / kSBuf) & 1, c, abort_flag);
-      uint32_t u[32];
+    uint32_t u[32];  // partial logits of the block being sent / held
+    auto fetch_and_send = [&](int jb) {
+      const int sbb = jb % kSBuf;
+      ok = ok && mbar_wait_warp(smem_u32(&sm.s_full[sbb]), (jb / kSBuf) & 1, c, abort_flag);
       if (ok) {
         tc_fence_after();
-        tmem_ld32(sbuf + 32 * hf, u);
+        tmem_ld32(tmem + lane_off + kColS + sbb * kBKey + 32 * hf, u);
         tmem_ld_wait();
       }
-      // my partial logits -> the peer's exchange buffer, completing on its x_full
-      ok = ok && mbar_wait_warp<true>(smem_u32(&sm.x_free), (j & 1) ^ 1, c, abort_flag);
+      // the peer has consumed block jb-1 from its exchange buffer
+      if (jb > 0) ok = ok && mbar_wait_warp<true>(smem_u32(&sm.x_free), (jb - 1) & 1, c, abort_flag);
       if (ok) {
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
           st_async_v4(x_remote + (((8 * hf + ch) * kH + h) << 4), u[4 * ch], u[4 * ch + 1],
                       u[4 * ch + 2], u[4 * ch + 3], xfull_remote);
       }
+    };
+    if (nblk > 0) {
+      if (armer) mbar_arrive_expect_tx(xfull, kH * kBKey * 4);  // phase 0 of x_full
+      fetch_and_send(0);
+    }
+    for (int j = 0; j < nblk; ++j) {
+      const int sb = j % kSBuf;
+      const uint32_t vmask = (uint32_t)(sm.mask[j] >> (32 * hf));
+      const uint32_t sbuf = tmem + lane_off + kColS + sb * kBKey;
       ok = ok && mbar_wait_warp<true>(xfull, j & 1, c, abort_flag);
       float v[32];
-      float bm = -INFINITY;
       if (ok) {
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
@@ -315,8 +347,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           v[4 * ch + 2] = __uint_as_float(u[4 * ch + 2]) + pr.z;
           v[4 * ch + 3] = __uint_as_float(u[4 * ch + 3]) + pr.w;
         }
+        // The arrive below is relaxed, so nothing but issue order keeps it behind
+        // the exchange-buffer loads: fold every loaded value into `dep` (real
+        // instructions that must wait for the load data) and make the arrive
+        // take it as an operand.
+        uint32_t dep = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) dep ^= __float_as_uint(v[i]);
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(xfree_remote);  // the values are in registers
+        if (lane == 0) mbar_arrive_remote_relaxed_after(xfree_remote, dep);
+        if (armer && j + 1 < nblk) mbar_arrive_expect_tx(xfull, kH * kBKey * 4);  // phase j+1
+      }
+      if (j + 1 < nblk) fetch_and_send(j + 1);
+      float bm = -INFINITY;
+      if (ok) {
         if (vmask != 0xffffffffu) {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
@@ -336,8 +380,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float m_new = fmaxf(m_run, bm);
         const float alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - m_new);
         if (j > 0 && __any_sync(0xffffffffu, m_run != -INFINITY)) {
-          // O must hold PV(j-1) before it is rescaled; each half owns 128 columns
-          ok = mbar_wait_warp(smem_u32(&sm.pv_done), (j - 1) & 1, c, abort_flag);
+          // O must hold PV(j-1) before it is rescaled; each half owns 128 columns.
+          // s_free[b] completes once per PV on buffer b; the phase before the one
+          // awaited is known complete (S(j-1) reused the buffer), so the parity
+          // test is unambiguous, and PVs complete in issue order.
+          ok = mbar_wait_warp(smem_u32(&sm.s_free[(j - 1) % kSBuf]), ((j - 1) / kSBuf) & 1, c,
+                              abort_flag);
           if (!ok) continue;
           tc_fence_after();
 #pragma unroll 1
@@ -369,7 +417,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     // ------------------------------- epilogue -------------------------------
     bool have = ok && nblk > 0;
-    if (have) have = mbar_wait_warp(smem_u32(&sm.pv_done), (nblk - 1) & 1, c, abort_flag);
+    if (have)  // PV(nblk-1) done, hence every PV (see the rescale wait above)
+      have = mbar_wait_warp(smem_u32(&sm.s_free[(nblk - 1) % kSBuf]), ((nblk - 1) / kSBuf) & 1, c,
+                            abort_flag);
     tc_fence_after();
     sm.red[nblk & 1][hf][h] = l_run;  // the buffer the last block's maxima did not use
     named_bar_sync(1, kSoftWarps * 32);

@@ -86,6 +86,14 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
 }
+// Remote arrive with no ordering of earlier memory operations; `dep` (unused
+// by the instruction) pins it after the computation of `dep` in issue order.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed_after(uint32_t cluster_bar,
+                                                                 uint32_t dep) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar),
+               "r"(dep)
+               : "memory");
+}
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

@@ -133,3 +133,23 @@ def test_cp_head_tail_shard_bit_identical():
     for part, rr in ((ht, rows.tolist()), (off, list(range(1024, 2048)))):
         for key in ("idx", "out", "m", "l"):
             assert torch.equal(part[key], full[key][:, rr]), key
+
+
+def test_attention_bit_deterministic_across_runs():
+    # the pipelined kernel must give bit-identical results run to run
+    dsa = lib()
+    wl = synth.WORKLOADS["dsv32_S4096"]
+    S, k = wl["S"], wl["topk"]
+    x = synth.make_inputs(wl, device=DEV)
+    p = params(dsa, wl)
+    o = empty_outputs(wl, S, torch.bfloat16)
+    ws = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_FORWARD) // 4, device=DEV)
+    dsa.forward(p, x["q_I"], x["k_I"], x["w"], x["q"], x["kv"], o["idx"], o["out"], o["m"], o["l"], ws)
+    torch.cuda.synchronize()
+    for _ in range(4):
+        r = empty_outputs(wl, S, torch.bfloat16)
+        dsa.sparse_attn_fwd(p, x["q"], x["kv"], o["idx"], r["out"], r["m"], r["l"])
+        torch.cuda.synchronize()
+        assert dsa.get_status() == 0
+        for key in ("out", "m", "l"):
+            assert torch.equal(r[key], o[key]), key
