@@ -32,6 +32,15 @@ int launch_indexer_tc(const Shape& s, const void* q_I, const void* k_I, const vo
                       cudaStream_t st);
 int launch_attn_fwd_tc(const Shape& s, const void* q, const void* kv, const int32_t* idx, void* out,
                        float* mx, float* sm, DevCtx c, cudaStream_t st);
+size_t bwd_tc_workspace(const Shape& s);
+size_t kl_tc_workspace(const Shape& s);
+int launch_attn_bwd_tc(const Shape& s, const void* q, const void* kv, const int32_t* idx,
+                       const void* out, const void* dout, const float* mx, const float* sm,
+                       void* dq, float* dkv, void* ws, DevCtx c, cudaStream_t st);
+int launch_kl_bwd_tc(const Shape& s, const void* q, const void* kv, const void* q_I,
+                     const void* k_I, const void* w, const int32_t* idx, const float* mx,
+                     const float* sm, float* loss, void* dq_I, float* dk_I, float* dw, void* ws,
+                     DevCtx c, cudaStream_t st);
 
 // ------------------------------ status word --------------------------------
 __device__ int g_status;
@@ -156,6 +165,12 @@ static int attn_fwd(const dsa_params* p, const Shape& s, const void* q, const vo
   return launch_simt_attn_fwd(s, false, q, kv, idx, out, mx, sm, c, st);
 }
 
+// the tensor-core backward: DeepSeek head shapes, k <= 2048 and a multiple of
+// 8 (the [rows*128][k] bf16 intermediates are read by TMA, 16-byte rows)
+static bool tc_bwd_shape(const dsa_params* p) {
+  return p->dtype == DSA_BF16 && tc_attn_shape(p) && p->topk <= 2048 && p->topk % 8 == 0;
+}
+
 static long long wave_rows(const dsa_params* p) {
   const long long total = p->B * p->S_q;
   long long w = p->wave_rows;
@@ -179,6 +194,8 @@ size_t dsa_workspace_size(const dsa_params* p, int which) {
   Shape s;
   if (check_params(p, &s) != DSA_OK) return 0;
   if (which == DSA_CALL_FORWARD) return (size_t)wave_rows(p) * (size_t)p->S_k * sizeof(float);
+  if (which == DSA_CALL_ATTN_BWD && tc_bwd_shape(p)) return bwd_tc_workspace(s);
+  if (which == DSA_CALL_KL_BWD && tc_bwd_shape(p) && tc_indexer_shape(p)) return kl_tc_workspace(s);
   // the exact (fp32) path accumulates dkv / dk_I in fp64 before adding them
   if (which == DSA_CALL_ATTN_BWD && p->dtype == DSA_FP32)
     return (size_t)(p->B * p->S_k * p->d_qk) * sizeof(double);
@@ -238,7 +255,17 @@ int dsa_sparse_attn_bwd(const dsa_params* p, const void* q, const void* kv, cons
   if (rc) return rc;
   if (!q || !kv || !idx || !out || !dout || !softmax_max || !softmax_sum || !dq || !dkv)
     return DSA_ERR_INVALID_ARG;
-  if (simt_smem_attn_bwd(s) > 200 * 1024) return DSA_ERR_UNSUPPORTED;
+  if (tc_bwd_shape(p)) {
+    if (!aligned16(q) || !aligned16(kv) || !aligned16(out) || !aligned16(dout) || !aligned16(dq) ||
+        !aligned16(dkv))
+      return DSA_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace)) return DSA_ERR_WORKSPACE;
+    DevCtx c;
+    if (!dev_ctx(&c)) return DSA_ERR_CUDA;
+    return launch_attn_bwd_tc(s, q, kv, idx, out, dout, softmax_max, softmax_sum, dq, dkv,
+                              workspace, c, (cudaStream_t)stream);
+  }
+  if (p->dtype == DSA_BF16 || simt_smem_attn_bwd(s) > 200 * 1024) return DSA_ERR_UNSUPPORTED;
   if (dsa_workspace_size(p, DSA_CALL_ATTN_BWD) > 0 && !aligned16(workspace)) return DSA_ERR_WORKSPACE;
   DevCtx c;
   if (!dev_ctx(&c)) return DSA_ERR_CUDA;
@@ -257,7 +284,17 @@ int dsa_indexer_kl_loss_bwd(const dsa_params* p, const void* q, const void* kv, 
   if (!q || !kv || !q_I || !k_I || !w || !idx || !softmax_max || !softmax_sum || !loss || !dq_I ||
       !dk_I || !dw)
     return DSA_ERR_INVALID_ARG;
-  if (simt_smem_kl(s) > 200 * 1024) return DSA_ERR_UNSUPPORTED;
+  if (tc_bwd_shape(p) && tc_indexer_shape(p)) {
+    if (!aligned16(q) || !aligned16(kv) || !aligned16(k_I) || !aligned16(dk_I) ||
+        ((uintptr_t)dq_I & 3u) != 0)
+      return DSA_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace)) return DSA_ERR_WORKSPACE;
+    DevCtx c;
+    if (!dev_ctx(&c)) return DSA_ERR_CUDA;
+    return launch_kl_bwd_tc(s, q, kv, q_I, k_I, w, idx, softmax_max, softmax_sum, loss, dq_I, dk_I,
+                            dw, workspace, c, (cudaStream_t)stream);
+  }
+  if (p->dtype == DSA_BF16 || simt_smem_kl(s) > 200 * 1024) return DSA_ERR_UNSUPPORTED;
   if (dsa_workspace_size(p, DSA_CALL_KL_BWD) > 0 && !aligned16(workspace)) return DSA_ERR_WORKSPACE;
   DevCtx c;
   if (!dev_ctx(&c)) return DSA_ERR_CUDA;

@@ -1,0 +1,882 @@
+// Backward of the sparse attention and the target side of the indexer KL loss
+// on tcgen05 (bf16 in, fp32 accumulate), DeepSeek-V3.2 shapes (128 heads,
+// d_qk 576, d_v 512).
+//
+// [DSA-32K] SparseFlashAttentionGrad: gather K_topk, recompute P, dP = dY V^T,
+// dS = P * (dP - FlashSoftmaxGrad(dY, O)), dQ = dS K_topk / sqrt(d),
+// dK = ScatterAdd(dS^T Q / sqrt(d)), dV = P^T dY.
+//
+// A token's operands (q 128x576, dO 128x512) and its accumulators (dQ
+// 128x576, a key block's dKV slice) do not fit one SM's shared or tensor
+// memory together, so the backward is split into GEMM-shaped passes with the
+// per-pair intermediates materialised in HBM (bf16, [rows][128][k]):
+//   rowdot  D[t,h]  = sum_e dO*O                                  (SIMT)
+//   scores  S, dP   per (token, 128-key tile) in TMEM; epilogue writes
+//           P = exp(scale*S - m)/l and scale*dS = scale*P*(dP - D)
+//   dq      dQ[t]   = (scale*dS) K_sel           per (token, 192-col tile)
+//   dkv     dKV_sel += (scale*dS)^T Q + P^T dO   per (token, key tile, col tile),
+//           scattered with fp32 vector reductions.
+// The same scores kernel in its logits-only form gives the head-summed
+// attention probabilities the indexer KL loss needs.
+#include <math.h>
+
+#include "dsa_common.cuh"
+
+namespace dsa {
+namespace bwd {
+
+constexpr int kH = 128, kDQK = 576, kDV = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------- rowdot ------------------------------------
+// One warp per (row, head): D = sum over the 512 value columns of dO * O.
+__global__ void rowdot_kernel(const __nv_bfloat16* __restrict__ dout,
+                              const __nv_bfloat16* __restrict__ out, float* __restrict__ D,
+                              long long nrh) {
+  const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= nrh) return;
+  const uint4* a = reinterpret_cast<const uint4*>(dout + w * kDV);
+  const uint4* b = reinterpret_cast<const uint4*>(out + w * kDV);
+  float acc = 0.f;
+#pragma unroll
+  for (int i = lane; i < kDV / 8; i += 32) {
+    const uint4 x = a[i], y = b[i];
+    const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&x);
+    const __nv_bfloat162* yp = reinterpret_cast<const __nv_bfloat162*>(&y);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 xf = __bfloat1622float2(xp[q]), yf = __bfloat1622float2(yp[q]);
+      acc = fmaf(xf.x, yf.x, fmaf(xf.y, yf.y, acc));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) D[w] = acc;
+}
+
+// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi), for two values packed
+// as bf16x2 (first value in the low half)
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+  hi = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+  lo = pack_bf16x2(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+}
+
+// ------------------------------- scores ------------------------------------
+// CTA = (row, 128-key tile).  warp 0: TMEM + MMA; warp 1: TMA of q / dO column
+// chunks (64 columns x 128 heads, 3-stage ring); warps 2..5: gather the tile's
+// 128 kv rows (all 576 columns, K-major SW128, 9 chunks), then the epilogue
+// (thread = head).
+constexpr int kSTile = 128;
+constexpr int kSThreads = 192;
+constexpr int kSStages = 3;
+struct __align__(1024) ScoresSmem {
+  uint8_t kv[9][kSTile * 128];     // 144 KB; reused as a [128 keys][129] fp32 transpose buffer
+  uint8_t a[kSStages][kH * 128];   // 48 KB
+  int32_t idx[kSTile];
+  uint32_t mask[kSTile / 32];
+  uint64_t a_full[kSStages], a_empty[kSStages], kv_full, done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <bool kGrad>
+__global__ void __launch_bounds__(kSThreads, 1)
+    scores_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __nv_bfloat16* __restrict__ kv, Shape s, const int32_t* __restrict__ idx,
+                  const float* __restrict__ mx, const float* __restrict__ lsum,
+                  const float* __restrict__ Dg, __nv_bfloat16* __restrict__ P_ws,
+                  __nv_bfloat16* __restrict__ Plo_ws, __nv_bfloat16* __restrict__ dS_ws,
+                  __nv_bfloat16* __restrict__ dSlo_ws,
+                  float* __restrict__ praw, int ntile,
+                  DevCtx c) {
+  extern __shared__ uint8_t smem_raw[];
+  ScoresSmem& sm = *reinterpret_cast<ScoresSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = blockIdx.x / ntile;
+  const int tile = blockIdx.x % ntile;
+  const long long b = row / s.S_q;
+  const int k = s.topk;
+  const int slot0 = tile * kSTile;
+  volatile int* abort_flag = &sm.abort;
+  constexpr int nA = kGrad ? 17 : 9;  // 9 q chunks (+ 8 dO chunks)
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSStages; ++i) {
+      mbar_init(smem_u32(&sm.a_full[i]), 1);
+      mbar_init(smem_u32(&sm.a_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&sm.kv_full), 128);
+    mbar_init(smem_u32(&sm.done), 1);
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x < kSTile) {
+    const int sl = slot0 + threadIdx.x;
+    int id = sl < k ? idx[row * k + sl] : -1;
+    if (id < -1 || id >= s.S_k) set_status(c, DSA_ERR_INDEX);
+    if (id < 0 || id >= s.S_k) id = -1;
+    sm.idx[threadIdx.x] = id;
+    const uint32_t bal = __ballot_sync(0xffffffffu, id >= 0);
+    if (lane == 0) sm.mask[threadIdx.x >> 5] = bal;
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 256);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const bool any = (sm.mask[0] | sm.mask[1] | sm.mask[2] | sm.mask[3]) != 0u;
+
+  if (any) {
+    if (warp == 1) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        if (kGrad) tma_prefetch_desc(&tm_do);
+        const int y = (int)(row * kH);
+        for (int i = 0; i < nA; ++i) {
+          const int st = i % kSStages;
+          if (!mbar_wait(smem_u32(&sm.a_empty[st]), ((i / kSStages) & 1) ^ 1, c, abort_flag)) break;
+          const uint32_t fb = smem_u32(&sm.a_full[st]);
+          mbar_arrive_expect_tx(fb, kH * 128);
+          if (i < 9) tma_load_2d(smem_u32(sm.a[st]), &tm_q, 64 * i, y, fb);
+          else tma_load_2d(smem_u32(sm.a[st]), &tm_do, 64 * (i - 9), y, fb);
+        }
+        for (int i = (nA > kSStages ? nA - kSStages : 0); i < nA; ++i)  // drain
+          mbar_wait(smem_u32(&sm.a_full[i % kSStages]), (i / kSStages) & 1, c, abort_flag);
+      }
+    } else if (warp >= 2) {
+      // gather: warp gw owns keys gw, gw+4, ...; lane = 16-byte chunk (72 per row)
+      const int gw = warp - 2;
+      const __nv_bfloat16* kvb = kv + b * s.S_k * (long long)kDQK;
+      const uint32_t kvs = smem_u32(sm.kv);
+#pragma unroll 1
+      for (int m0 = 0; m0 < 32; m0 += 8) {
+        uint4 r[8][3];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const int key = gw + 4 * (m0 + m);
+          const int id = sm.idx[key] < 0 ? 0 : sm.idx[key];
+          const uint4* src = reinterpret_cast<const uint4*>(kvb + (long long)id * kDQK);
+#pragma unroll
+          for (int q = 0; q < 3; ++q)
+            if (lane + 32 * q < 72) r[m][q] = __ldg(src + lane + 32 * q);
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const int key = gw + 4 * (m0 + m);
+#pragma unroll
+          for (int q = 0; q < 3; ++q) {
+            const int ch = lane + 32 * q;
+            if (ch < 72) {
+              const int g = ch >> 3, cc = ch & 7;
+              const uint32_t dst = kvs + g * (kSTile * 128) + key * 128 + ((cc ^ (key & 7)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(r[m][q].x),
+                           "r"(r[m][q].y), "r"(r[m][q].z), "r"(r[m][q].w)
+                           : "memory");
+            }
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&sm.kv_full));
+    } else if (lane == 0) {
+      // MMA: S (TMEM cols 0..127) and dP (cols 128..255), M=128 heads, N=128 keys
+      constexpr uint32_t idesc = idesc_bf16(128, kSTile, false, false);
+      bool ok = mbar_wait(smem_u32(&sm.kv_full), 0, c, abort_flag);
+      const uint32_t kvs = smem_u32(sm.kv);
+      for (int i = 0; ok && i < nA; ++i) {
+        const int st = i % kSStages;
+        if (!mbar_wait(smem_u32(&sm.a_full[st]), (i / kSStages) & 1, c, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (i < 9 ? 0u : 128u);
+        const int kc = i < 9 ? i : i - 9;
+        const uint32_t a0 = smem_u32(sm.a[st]);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ss(d, sdesc(a0 + kk * 32, 16, 1024, kSw128),
+                      sdesc(kvs + kc * (kSTile * 128) + kk * 32, 16, 1024, kSw128), idesc,
+                      (i != 0 && i != 9) || kk > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&sm.a_empty[st]));
+      }
+      mma_commit(smem_u32(&sm.done));
+    }
+  }
+  if (warp >= 2) {
+    // --------------------------- epilogue: thread = head ---------------------------
+    const int quad = warp & 3;
+    const int h = quad * 32 + lane;
+    const long long rh = row * kH + h;
+    bool have = any && mbar_wait_warp(smem_u32(&sm.done), 0, c, abort_flag);
+    tc_fence_after();
+    const float mh = mx[rh] * kLog2e;
+    const float lv = lsum[rh];
+    const float linv = lv > 0.f ? 1.f / lv : 0.f;
+    const float sl2e = s.scale * kLog2e;
+    const float Dh = kGrad ? Dg[rh] : 0.f;
+    float* T = reinterpret_cast<float*>(sm.kv);  // colsum mode: [128 heads][128 keys]
+#pragma unroll 1
+    for (int cc = 0; cc < kSTile; cc += 32) {
+      uint32_t sv[32], dv[32];
+      if (have) {
+        tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + cc, sv);
+        if (kGrad) tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + 128 + cc, dv);
+        tmem_ld_wait();
+      }
+      const uint32_t vm = sm.mask[cc >> 5];
+      float p[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        p[i] = (have && ((vm >> i) & 1u)) ? ex2(fmaf(__uint_as_float(sv[i]), sl2e, -mh)) * linv : 0.f;
+      if (kGrad) {
+        // P and scale*dS as bf16 pairs hi + lo, hi = bf16(x), lo = bf16(x - hi):
+        // the later passes contract both halves, so the products carry ~16
+        // mantissa bits of P and dS instead of 8
+        uint4 ph[4], pl[4], dh[4], dl[4];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float d0 = have ? p[2 * i] * (__uint_as_float(dv[2 * i]) - Dh) * s.scale : 0.f;
+          const float d1 = have ? p[2 * i + 1] * (__uint_as_float(dv[2 * i + 1]) - Dh) * s.scale : 0.f;
+          split_bf16x2(p[2 * i], p[2 * i + 1], reinterpret_cast<uint32_t*>(ph)[i],
+                       reinterpret_cast<uint32_t*>(pl)[i]);
+          split_bf16x2(d0, d1, reinterpret_cast<uint32_t*>(dh)[i], reinterpret_cast<uint32_t*>(dl)[i]);
+        }
+        const long long o = rh * k + slot0 + cc;
+        uint4* o_ph = reinterpret_cast<uint4*>(P_ws + o);
+        uint4* o_pl = reinterpret_cast<uint4*>(Plo_ws + o);
+        uint4* o_dh = reinterpret_cast<uint4*>(dS_ws + o);
+        uint4* o_dl = reinterpret_cast<uint4*>(dSlo_ws + o);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (slot0 + cc + 8 * i < k) {  // k is a multiple of 8
+            o_ph[i] = ph[i];
+            o_pl[i] = pl[i];
+            o_dh[i] = dh[i];
+            o_dl[i] = dl[i];
+          }
+        }
+      } else {
+        // transpose through shared memory, [key][head] with a 129-float row
+        // pitch (conflict-free writes by head and reads by key)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) T[(cc + i) * (kH + 1) + h] = p[i];
+      }
+    }
+    if (!kGrad) {
+      named_bar_sync(1, 128);
+      const int key = h;  // thread = key: sum its row over the 128 heads
+      float acc = 0.f;
+      for (int hh = 0; hh < kH; ++hh) acc += T[key * (kH + 1) + hh];
+      if (slot0 + key < k) praw[row * k + slot0 + key] = acc;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// --------------------------------- dq ---------------------------------------
+// CTA = (row, 192-column tile of dQ).  dQ[t, :, cols] = sum over key chunks of
+// (scale*dS)[128 heads x 64 keys] * K_sel[64 keys x 192 cols], with scale*dS
+// taken as its bf16 pair hi + lo (two MMAs per chunk on the same K tile).
+// warp 0: MMA; warp 1: TMA of the dS chunks; warps 2..5: gather the 64 kv
+// rows' 192 columns (MN-major SW128: 3 atoms of 64 columns), then the epilogue.
+constexpr int kQStages = 3;
+constexpr int kQN = 192;
+struct __align__(1024) DqSmem {
+  uint8_t a[kQStages][2][kH * 128];     // dS hi, lo chunks: 128 heads x 64 keys, K-major
+  uint8_t bm[kQStages][3 * 64 * 128];   // 64 keys x 192 cols, MN-major
+  int32_t idx[2048];
+  uint64_t full[kQStages], empty[kQStages], done;
+  uint32_t tmem_base;
+  int abort;
+  int last;
+};
+
+__global__ void __launch_bounds__(192, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tm_ds, const __grid_constant__ CUtensorMap tm_dslo,
+              const __nv_bfloat16* __restrict__ kv,
+              Shape s, const int32_t* __restrict__ idx, __nv_bfloat16* __restrict__ dq, DevCtx c) {
+  extern __shared__ uint8_t smem_raw[];
+  DqSmem& sm = *reinterpret_cast<DqSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = blockIdx.x / 3;
+  const int nt = blockIdx.x % 3;
+  const long long b = row / s.S_q;
+  const int k = s.topk;
+  volatile int* abort_flag = &sm.abort;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kQStages; ++i) {
+      mbar_init(smem_u32(&sm.full[i]), 1 + 128);
+      mbar_init(smem_u32(&sm.empty[i]), 1);
+    }
+    mbar_init(smem_u32(&sm.done), 1);
+    sm.abort = 0;
+    sm.last = -1;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  int last = -1;
+  for (int i = threadIdx.x; i < k; i += blockDim.x) {
+    int id = idx[row * k + i];
+    if (id < 0 || id >= s.S_k) id = -1;
+    else last = i;
+    sm.idx[i] = id;
+  }
+  if (last >= 0) atomicMax(&sm.last, last);
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 256);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const int nch = (sm.last + 64) / 64;
+
+  if (warp == 1) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_ds);
+      tma_prefetch_desc(&tm_dslo);
+      for (int ch = 0; ch < nch; ++ch) {
+        const int st = ch % kQStages;
+        if (!mbar_wait(smem_u32(&sm.empty[st]), ((ch / kQStages) & 1) ^ 1, c, abort_flag)) break;
+        const uint32_t fb = smem_u32(&sm.full[st]);
+        mbar_arrive_expect_tx(fb, 2 * kH * 128);
+        tma_load_2d(smem_u32(sm.a[st][0]), &tm_ds, 64 * ch, (int)(row * kH), fb);
+        tma_load_2d(smem_u32(sm.a[st][1]), &tm_dslo, 64 * ch, (int)(row * kH), fb);
+      }
+      for (int ch = (nch > kQStages ? nch - kQStages : 0); ch < nch; ++ch)
+        mbar_wait(smem_u32(&sm.full[ch % kQStages]), (ch / kQStages) & 1, c, abort_flag);
+    }
+  } else if (warp >= 2) {
+    const int gw = warp - 2;
+    const __nv_bfloat16* kvb = kv + b * s.S_k * (long long)kDQK + kQN * nt;
+    for (int ch = 0; ch < nch; ++ch) {
+      const int st = ch % kQStages;
+      if (!mbar_wait_warp(smem_u32(&sm.empty[st]), ((ch / kQStages) & 1) ^ 1, c, abort_flag)) break;
+      uint4 r[16];
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const int key = gw + 4 * m;
+        const int sl = 64 * ch + key;
+        const int id = (sl < k && sm.idx[sl] >= 0) ? sm.idx[sl] : 0;
+        if (lane < 24) r[m] = __ldg(reinterpret_cast<const uint4*>(kvb + (long long)id * kDQK) + lane);
+      }
+      const uint32_t bs = smem_u32(sm.bm[st]);
+      if (lane < 24) {
+        const int at = lane >> 3, cc = lane & 7;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const int key = gw + 4 * m;
+          const uint32_t dst = bs + at * 8192 + key * 128 + ((cc ^ (key & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(r[m].x),
+                       "r"(r[m].y), "r"(r[m].z), "r"(r[m].w)
+                       : "memory");
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&sm.full[st]));
+    }
+  } else if (lane == 0) {
+    constexpr uint32_t idesc = idesc_bf16(128, kQN, false, true);
+    for (int ch = 0; ch < nch; ++ch) {
+      const int st = ch % kQStages;
+      if (!mbar_wait(smem_u32(&sm.full[st]), (ch / kQStages) & 1, c, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t b0 = smem_u32(sm.bm[st]);
+#pragma unroll
+      for (int hl = 0; hl < 2; ++hl) {
+        const uint32_t a0 = smem_u32(sm.a[st][hl]);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ss(tmem, sdesc(a0 + kk * 32, 16, 1024, kSw128),
+                      sdesc(b0 + kk * 2048, 8192, 1024, kSw128), idesc,
+                      (ch > 0 || hl > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(smem_u32(&sm.empty[st]));
+    }
+    mma_commit(smem_u32(&sm.done));
+  }
+  if (warp >= 2) {
+    const int quad = warp & 3;
+    const int h = quad * 32 + lane;
+    bool have = nch > 0 && mbar_wait_warp(smem_u32(&sm.done), 0, c, abort_flag);
+    tc_fence_after();
+    __nv_bfloat16* dst = dq + (row * kH + h) * (long long)kDQK + kQN * nt;
+#pragma unroll 1
+    for (int cc = 0; cc < kQN; cc += 32) {
+      uint32_t v[32];
+      if (have) {
+        tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + cc, v);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0u;
+      }
+      uint4 pk[4];
+      uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) pw[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+      uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d4[i] = pk[i];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// --------------------------------- dkv --------------------------------------
+// CTA = (row, 128-key tile, column tile n: [0,256) | [256,512) | [512,576)).
+// D[128 keys x N] = (scale*dS)^T Q (+ P^T dO for value columns), contracted
+// over the 128 heads in four chunks of 32 through a 3-stage TMA ring.  P and
+// scale*dS enter as bf16 pairs hi + lo (a single bf16 rounding of P or dS
+// would leave the accumulated dKV of early keys about 0.1 off at this size).
+// Both operands are MN-major straight from TMA boxes (64 keys or 64 columns
+// by 32 heads).  warp 1 lane 0: TMA; warp 0 lane 0: MMA; then all four warps
+// drain TMEM (thread = key) and scatter-add their rows into dkv with vector
+// reductions.
+constexpr int kVStages = 3;
+constexpr int kVHeads = 32;                 // heads per stage
+constexpr int kVBox = 64 * kVHeads * 2;     // 4 KB: 64 keys (or columns) x 32 heads
+struct __align__(1024) DkvSmem {
+  uint8_t a[kVStages][4][2][kVBox];         // [dS hi, dS lo, P hi, P lo][key half]
+  uint8_t bq[kVStages][4][kVBox];           // q columns, 4 boxes of 64
+  uint8_t bo[kVStages][4][kVBox];           // dO columns
+  int32_t idx[128];
+  uint32_t mask[4];
+  uint64_t full[kVStages], empty[kVStages], done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__global__ void __launch_bounds__(128, 1)
+    dkv_kernel(const __grid_constant__ CUtensorMap tm_ds, const __grid_constant__ CUtensorMap tm_dslo,
+               const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_plo,
+               const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+               Shape s, const int32_t* __restrict__ idx, float* __restrict__ dkv, int ntile,
+               DevCtx c) {
+  extern __shared__ uint8_t smem_raw[];
+  DkvSmem& sm = *reinterpret_cast<DkvSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = blockIdx.x % 3;
+  const int tile = (blockIdx.x / 3) % ntile;
+  const long long row = blockIdx.x / (3 * ntile);
+  const long long b = row / s.S_q;
+  const int k = s.topk;
+  const int slot0 = tile * 128;
+  const int N = nt < 2 ? 256 : 64;
+  const int ncb = N / 64;
+  const bool withV = nt < 2;
+  const int nA = withV ? 4 : 2;             // A operands per stage
+  constexpr int nChunk = kH / kVHeads;
+  volatile int* abort_flag = &sm.abort;
+  {
+    const int sl = slot0 + threadIdx.x;
+    int id = sl < k ? idx[row * k + sl] : -1;
+    if (id < 0 || id >= s.S_k) id = -1;
+    sm.idx[threadIdx.x] = id;
+    const uint32_t bal = __ballot_sync(0xffffffffu, id >= 0);
+    if (lane == 0) sm.mask[warp] = bal;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(smem_u32(&sm.full[i]), 1);
+      mbar_init(smem_u32(&sm.empty[i]), 1);
+    }
+    mbar_init(smem_u32(&sm.done), 1);
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 256);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const bool any = (sm.mask[0] | sm.mask[1] | sm.mask[2] | sm.mask[3]) != 0u;
+  if (any && warp == 1 && lane == 0) {
+    const CUtensorMap* am[4] = {&tm_ds, &tm_dslo, &tm_p, &tm_plo};
+    const uint32_t bytes = (uint32_t)(nA * 2 + (withV ? 2 : 1) * ncb) * kVBox;
+    for (int ch = 0; ch < nChunk; ++ch) {
+      const int st = ch % kVStages;
+      if (!mbar_wait(smem_u32(&sm.empty[st]), ((ch / kVStages) & 1) ^ 1, c, abort_flag)) break;
+      const uint32_t fb = smem_u32(&sm.full[st]);
+      mbar_arrive_expect_tx(fb, bytes);
+      const int y = (int)(row * kH) + kVHeads * ch;
+      for (int o = 0; o < nA; ++o)
+        for (int kk = 0; kk < 2; ++kk)
+          tma_load_2d(smem_u32(sm.a[st][o][kk]), am[o], slot0 + 64 * kk, y, fb);
+      for (int cb = 0; cb < ncb; ++cb) {
+        tma_load_2d(smem_u32(sm.bq[st][cb]), &tm_q, 256 * nt + 64 * cb, y, fb);
+        if (withV) tma_load_2d(smem_u32(sm.bo[st][cb]), &tm_do, 256 * nt + 64 * cb, y, fb);
+      }
+    }
+    for (int ch = nChunk - kVStages; ch < nChunk; ++ch)  // drain: no copy left in flight
+      mbar_wait(smem_u32(&sm.full[ch % kVStages]), (ch / kVStages) & 1, c, abort_flag);
+  } else if (any && warp == 0 && lane == 0) {
+    const uint32_t idesc = idesc_bf16(128, N, true, true);
+    for (int ch = 0; ch < nChunk; ++ch) {
+      const int st = ch % kVStages;
+      if (!mbar_wait(smem_u32(&sm.full[st]), (ch / kVStages) & 1, c, abort_flag)) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int o = 0; o < nA; ++o) {
+        const uint32_t a0 = smem_u32(sm.a[st][o][0]);
+        const uint32_t b0 = smem_u32(o < 2 ? sm.bq[st][0] : sm.bo[st][0]);
+#pragma unroll
+        for (int kk = 0; kk < kVHeads / 16; ++kk)
+          mma_bf16_ss(tmem, sdesc(a0 + kk * 2048, kVBox, 1024, kSw128),
+                      sdesc(b0 + kk * 2048, kVBox, 1024, kSw128), idesc,
+                      (ch > 0 || o > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(smem_u32(&sm.empty[st]));
+    }
+    mma_commit(smem_u32(&sm.done));
+  }
+  if (any) {
+    const int key = warp * 32 + lane;
+    const bool have = mbar_wait_warp(smem_u32(&sm.done), 0, c, abort_flag);
+    tc_fence_after();
+    const int id = sm.idx[key];
+    float* dst = dkv + (b * s.S_k + (id < 0 ? 0 : id)) * (long long)kDQK + 256 * nt;
+#pragma unroll 1
+    for (int cc = 0; cc < N; cc += 32) {
+      uint32_t v[32];
+      if (have) {
+        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + cc, v);
+        tmem_ld_wait();
+        if (id >= 0) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            red_add_v4(dst + cc + i, __uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                       __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// ------------------------- indexer KL loss (SIMT) ---------------------------
+// [DSA-32K] SparseLightningIndexerGradKLLoss, per query row:
+//   p  = praw / sum(praw)       (head-summed attention probabilities,
+//                                L1-normalised over the selected keys)
+//   S_j = q_I,j . k_I[idx]      (stored: the later passes need it)
+//   I  = sum_j w_j ReLU(S_j),  pi = Softmax(I) over the selected keys
+//   loss += sum p (log p - log pi),  dI = pi - p   (stored)
+// then  dS_j = dI w_j [S_j > 0],  dw_j = sum dI ReLU(S_j),
+//       dq_I = dS K_sel (kl_dq_kernel),  dk_I[idx] += dS^T q_I (kl_dk_kernel).
+constexpr int kHI = 64, kDI = 128;
+__global__ void __launch_bounds__(256)
+    kl_main_kernel(Shape s, const __nv_bfloat16* __restrict__ q_I, const __nv_bfloat16* __restrict__ k_I,
+                   const __nv_bfloat16* __restrict__ w, const int32_t* __restrict__ idx,
+                   const float* __restrict__ praw, float* __restrict__ loss,
+                   float* __restrict__ S_ws, float* __restrict__ dI_ws, DevCtx c) {
+  extern __shared__ float sh[];
+  const int k = s.topk;
+  float* qs = sh;                       // [64][128]
+  float* ws = qs + kHI * kDI;           // [64]
+  float* pv = ws + kHI;                 // [k] target p
+  float* Iv = pv + k;                   // [k] indexer logits
+  float* red = Iv + k;                  // [32]
+  const long long row = blockIdx.x;
+  const long long b = row / s.S_q;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kHI * kDI; i += 256) qs[i] = __bfloat162float(q_I[row * kHI * kDI + i]);
+  for (int i = tid; i < kHI; i += 256) ws[i] = __bfloat162float(w[row * kHI + i]);
+  float psum = 0.f;
+  for (int i = tid; i < k; i += 256) {
+    const int id = idx[row * k + i];
+    const float pr = (id >= 0 && id < s.S_k) ? praw[row * k + i] : 0.f;
+    pv[i] = pr;
+    psum += pr;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
+  if (lane == 0) red[warp] = psum;
+  __syncthreads();
+  float P = 0.f;
+  for (int i = 0; i < 8; ++i) P += red[i];
+  const float pinv = P > 0.f ? 1.f / P : 0.f;
+  float* Srow = S_ws + row * (long long)kHI * k;
+  float imax = -INFINITY;
+  for (int i = tid; i < k; i += 256) {
+    pv[i] *= pinv;
+    const int id = idx[row * k + i];
+    float I = -INFINITY;
+    if (id >= 0 && id < s.S_k) {
+      const uint4* kr = reinterpret_cast<const uint4*>(k_I + (b * s.S_k + id) * kDI);
+      float kf[kDI];
+#pragma unroll
+      for (int q = 0; q < kDI / 8; ++q) {
+        const uint4 u = __ldg(kr + q);
+        const __nv_bfloat162* hp = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(hp[e]);
+          kf[8 * q + 2 * e] = f.x;
+          kf[8 * q + 2 * e + 1] = f.y;
+        }
+      }
+      I = 0.f;
+#pragma unroll 1
+      for (int j = 0; j < kHI; ++j) {
+        const float* qj = qs + j * kDI;
+        float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+        for (int d = 0; d < kDI; d += 2) {
+          d0 = fmaf(qj[d], kf[d], d0);
+          d1 = fmaf(qj[d + 1], kf[d + 1], d1);
+        }
+        const float S = d0 + d1;
+        Srow[(long long)j * k + i] = S;
+        I = fmaf(ws[j], fmaxf(S, 0.f), I);
+      }
+    } else {
+      for (int j = 0; j < kHI; ++j) Srow[(long long)j * k + i] = 0.f;
+    }
+    Iv[i] = I;
+    imax = fmaxf(imax, I);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) imax = fmaxf(imax, __shfl_xor_sync(0xffffffffu, imax, o));
+  __syncthreads();
+  if (lane == 0) red[warp] = imax;
+  __syncthreads();
+  float Im = red[0];
+  for (int i = 1; i < 8; ++i) Im = fmaxf(Im, red[i]);
+  float es = 0.f;
+  for (int i = tid; i < k; i += 256)
+    if (Iv[i] != -INFINITY) es += expf(Iv[i] - Im);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) es += __shfl_xor_sync(0xffffffffu, es, o);
+  __syncthreads();
+  if (lane == 0) red[warp] = es;
+  __syncthreads();
+  float E = 0.f;
+  for (int i = 0; i < 8; ++i) E += red[i];
+  const float lse = Im + logf(E);
+  float lpart = 0.f;
+  for (int i = tid; i < k; i += 256) {
+    float di = 0.f;
+    if (Iv[i] != -INFINITY) {
+      const float logpi = Iv[i] - lse;
+      if (pv[i] > 0.f) lpart += pv[i] * (logf(pv[i]) - logpi);
+      di = expf(logpi) - pv[i];
+    }
+    dI_ws[row * k + i] = di;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lpart += __shfl_xor_sync(0xffffffffu, lpart, o);
+  __syncthreads();
+  if (lane == 0) red[warp] = lpart;
+  __syncthreads();
+  if (tid == 0 && Im != -INFINITY) {
+    float L = 0.f;
+    for (int i = 0; i < 8; ++i) L += red[i];
+    atomicAdd(loss, L);
+  }
+}
+
+// dk_I[idx_i, :] += sum_j dS_ij q_I[t, j, :],  dS_ij = dI_i w_j [S_ij > 0].
+// CTA = row, thread = key slot; vector reductions into dk_I.
+__global__ void __launch_bounds__(256)
+    kl_dk_kernel(Shape s, const __nv_bfloat16* __restrict__ q_I, const __nv_bfloat16* __restrict__ w,
+                 const int32_t* __restrict__ idx, const float* __restrict__ S_ws,
+                 const float* __restrict__ dI_ws, float* __restrict__ dk_I) {
+  __shared__ float qs[kHI * kDI];
+  __shared__ float wsh[kHI];
+  const long long row = blockIdx.x;
+  const long long b = row / s.S_q;
+  const int k = s.topk;
+  for (int i = threadIdx.x; i < kHI * kDI; i += 256) qs[i] = __bfloat162float(q_I[row * kHI * kDI + i]);
+  if (threadIdx.x < kHI) wsh[threadIdx.x] = __bfloat162float(w[row * kHI + threadIdx.x]);
+  __syncthreads();
+  const float* Srow = S_ws + row * (long long)kHI * k;
+  for (int i = threadIdx.x; i < k; i += 256) {
+    const int id = idx[row * k + i];
+    if (id < 0 || id >= s.S_k) continue;
+    const float di = dI_ws[row * k + i];
+    float* dkr = dk_I + (b * s.S_k + id) * kDI;
+#pragma unroll 1
+    for (int d0 = 0; d0 < kDI; d0 += 32) {
+      float acc[32];
+#pragma unroll
+      for (int d = 0; d < 32; ++d) acc[d] = 0.f;
+      for (int j = 0; j < kHI; ++j) {
+        if (!(Srow[(long long)j * k + i] > 0.f)) continue;
+        const float g = di * wsh[j];
+        const float* qj = qs + j * kDI + d0;
+#pragma unroll
+        for (int d = 0; d < 32; ++d) acc[d] = fmaf(g, qj[d], acc[d]);
+      }
+#pragma unroll
+      for (int d = 0; d < 32; d += 4) red_add_v4(dkr + d0 + d, acc[d], acc[d + 1], acc[d + 2], acc[d + 3]);
+    }
+  }
+}
+
+// dq_I[t, j, :] = sum_i dS_ij k_I[idx_i, :] and dw[t, j] = sum_i dI_i ReLU(S_ij).
+// CTA = row; thread = (head j = tid/4, 32 dims at 32*(tid%4)).
+__global__ void __launch_bounds__(256)
+    kl_dq_kernel(Shape s, const __nv_bfloat16* __restrict__ k_I, const __nv_bfloat16* __restrict__ w,
+                 const int32_t* __restrict__ idx, const float* __restrict__ S_ws,
+                 const float* __restrict__ dI_ws, __nv_bfloat16* __restrict__ dq_I,
+                 float* __restrict__ dw) {
+  const long long row = blockIdx.x;
+  const long long b = row / s.S_q;
+  const int k = s.topk;
+  const int j = threadIdx.x >> 2, d0 = 32 * (threadIdx.x & 3);
+  const float wj = __bfloat162float(w[row * kHI + j]);
+  const float* Sr = S_ws + (row * kHI + j) * (long long)k;
+  const float* dIr = dI_ws + row * k;
+  float acc[32];
+#pragma unroll
+  for (int d = 0; d < 32; ++d) acc[d] = 0.f;
+  float dwacc = 0.f;
+  for (int i = 0; i < k; ++i) {
+    const int id = idx[row * k + i];
+    if (id < 0 || id >= s.S_k) continue;
+    const float S = Sr[i];
+    if (!(S > 0.f)) continue;
+    const float di = dIr[i];
+    dwacc = fmaf(di, S, dwacc);
+    const float g = di * wj;
+    const uint4* kr = reinterpret_cast<const uint4*>(k_I + (b * s.S_k + id) * kDI + d0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = __ldg(kr + q);
+      const __nv_bfloat162* hp = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(hp[e]);
+        acc[8 * q + 2 * e] = fmaf(g, f.x, acc[8 * q + 2 * e]);
+        acc[8 * q + 2 * e + 1] = fmaf(g, f.y, acc[8 * q + 2 * e + 1]);
+      }
+    }
+  }
+  __nv_bfloat16* o = dq_I + (row * kHI + j) * kDI + d0;
+#pragma unroll
+  for (int d = 0; d < 32; d += 2) *reinterpret_cast<__nv_bfloat162*>(o + d) = __floats2bfloat162_rn(acc[d], acc[d + 1]);
+  if ((threadIdx.x & 3) == 0) dw[row * kHI + j] = dwacc;
+}
+
+}  // namespace bwd
+
+bool make_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
+                       uint32_t box_cols, uint32_t box_rows, int swizzle_bytes);
+
+// workspace layout of the bf16 attention backward: P_hi, P_lo,
+// (scale*dS)_hi, (scale*dS)_lo [rows*128][k] bf16, then D [rows*128] fp32
+size_t bwd_tc_workspace(const Shape& s) {
+  const size_t rh = (size_t)s.B * s.S_q * bwd::kH;
+  return 4 * rh * (size_t)s.topk * 2 + rh * 4 + 256;
+}
+size_t kl_tc_workspace(const Shape& s) {
+  const size_t rows = (size_t)s.B * s.S_q;
+  return 2 * rows * (size_t)s.topk * 4 + rows * bwd::kHI * (size_t)s.topk * 4 + 256;
+}
+
+template <typename K>
+static bool set_smem(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) ==
+         cudaSuccess;
+}
+
+int launch_attn_bwd_tc(const Shape& s, const void* q, const void* kv, const int32_t* idx,
+                       const void* out, const void* dout, const float* mx, const float* sm,
+                       void* dq, float* dkv, void* ws, DevCtx c, cudaStream_t st) {
+  using namespace bwd;
+  const long long rows = (long long)s.B * s.S_q, rh = rows * kH;
+  const int k = s.topk;
+  __nv_bfloat16* P_ws = (__nv_bfloat16*)ws;
+  __nv_bfloat16* Plo_ws = P_ws + rh * k;
+  __nv_bfloat16* dS_ws = Plo_ws + rh * k;
+  __nv_bfloat16* dSlo_ws = dS_ws + rh * k;
+  float* D = (float*)(dSlo_ws + rh * k);
+  const int ntile = (k + 127) / 128;
+  // D = rowsum(dO * O)
+  rowdot_kernel<<<(unsigned)((rh * 32 + 255) / 256), 256, 0, st>>>(
+      (const __nv_bfloat16*)dout, (const __nv_bfloat16*)out, D, rh);
+  CUtensorMap tq, tdo, tds, tdslo, tds2, tdslo2, tp2, tplo2, tq2, tdo2;
+  if (!make_tmap_2d_bf16(&tq, q, rh, kDQK, 64, kH, 128)) return DSA_ERR_CUDA;
+  if (!make_tmap_2d_bf16(&tdo, dout, rh, kDV, 64, kH, 128)) return DSA_ERR_CUDA;
+  if (!make_tmap_2d_bf16(&tds, dS_ws, rh, k, 64, kH, 128)) return DSA_ERR_CUDA;
+  if (!make_tmap_2d_bf16(&tdslo, dSlo_ws, rh, k, 64, kH, 128)) return DSA_ERR_CUDA;
+  if (!make_tmap_2d_bf16(&tds2, dS_ws, rh, k, 64, kVHeads, 128)) return DSA_ERR_CUDA;
+  if (!make_tmap_2d_bf16(&tdslo2, dSlo_ws, rh, k, 64, kVHeads, 128)) return DSA_ERR_CUDA;
+  if (!make_tmap_2d_bf16(&tp2, P_ws, rh, k, 64, kVHeads, 128)) return DSA_ERR_CUDA;
+  if (!make_tmap_2d_bf16(&tplo2, Plo_ws, rh, k, 64, kVHeads, 128)) return DSA_ERR_CUDA;
+  if (!make_tmap_2d_bf16(&tq2, q, rh, kDQK, 64, kVHeads, 128)) return DSA_ERR_CUDA;
+  if (!make_tmap_2d_bf16(&tdo2, dout, rh, kDV, 64, kVHeads, 128)) return DSA_ERR_CUDA;
+  const size_t s1 = sizeof(ScoresSmem) + 1024, s2 = sizeof(DqSmem) + 1024, s3 = sizeof(DkvSmem) + 1024;
+  if (!set_smem(scores_kernel<true>, s1) || !set_smem(dq_kernel, s2) || !set_smem(dkv_kernel, s3))
+    return DSA_ERR_CUDA;
+  scores_kernel<true><<<(unsigned)(rows * ntile), kSThreads, s1, st>>>(
+      tq, tdo, (const __nv_bfloat16*)kv, s, idx, mx, sm, D, P_ws, Plo_ws, dS_ws, dSlo_ws, nullptr,
+      ntile, c);
+  dq_kernel<<<(unsigned)(rows * 3), 192, s2, st>>>(tds, tdslo, (const __nv_bfloat16*)kv, s, idx,
+                                                    (__nv_bfloat16*)dq, c);
+  dkv_kernel<<<(unsigned)(rows * ntile * 3), 128, s3, st>>>(tds2, tdslo2, tp2, tplo2, tq2, tdo2, s,
+                                                             idx, dkv, ntile, c);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+int launch_kl_bwd_tc(const Shape& s, const void* q, const void* kv, const void* q_I,
+                     const void* k_I, const void* w, const int32_t* idx, const float* mx,
+                     const float* sm, float* loss, void* dq_I, float* dk_I, float* dw, void* ws,
+                     DevCtx c, cudaStream_t st) {
+  using namespace bwd;
+  const long long rows = (long long)s.B * s.S_q, rh = rows * kH;
+  const int k = s.topk;
+  float* praw = (float*)ws;
+  float* dI = praw + rows * k;
+  float* Sw = dI + rows * k;
+  const int ntile = (k + 127) / 128;
+  CUtensorMap tq;
+  if (!make_tmap_2d_bf16(&tq, q, rh, kDQK, 64, kH, 128)) return DSA_ERR_CUDA;
+  const size_t s1 = sizeof(ScoresSmem) + 1024;
+  if (!set_smem(scores_kernel<false>, s1)) return DSA_ERR_CUDA;
+  scores_kernel<false><<<(unsigned)(rows * ntile), kSThreads, s1, st>>>(
+      tq, tq, (const __nv_bfloat16*)kv, s, idx, mx, sm, nullptr, nullptr, nullptr, nullptr, nullptr,
+      praw, ntile, c);
+  const size_t sk = sizeof(float) * (size_t)(kHI * kDI + kHI + 2 * k + 32);
+  if (!set_smem(kl_main_kernel, sk)) return DSA_ERR_CUDA;
+  kl_main_kernel<<<(unsigned)rows, 256, sk, st>>>(s, (const __nv_bfloat16*)q_I,
+                                                  (const __nv_bfloat16*)k_I,
+                                                  (const __nv_bfloat16*)w, idx, praw, loss, Sw, dI,
+                                                  c);
+  kl_dk_kernel<<<(unsigned)rows, 256, 0, st>>>(s, (const __nv_bfloat16*)q_I,
+                                               (const __nv_bfloat16*)w, idx, Sw, dI, dk_I);
+  kl_dq_kernel<<<(unsigned)rows, 256, 0, st>>>(s, (const __nv_bfloat16*)k_I,
+                                               (const __nv_bfloat16*)w, idx, Sw, dI,
+                                               (__nv_bfloat16*)dq_I, dw);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+}  // namespace dsa

@@ -279,6 +279,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+// dst[0..3] += {a,b,c,d} in global memory (fp32 vector reduction, no return)
+__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
 // Shared-memory matrix descriptor (tcgen05): start, leading / stride byte
 // offsets, fixed version 1, swizzle layout (0 none, 2 = 128B, 4 = 64B, 6 = 32B).
 constexpr uint32_t kSw128 = 2, kSw64 = 4;

@@ -69,3 +69,25 @@ def test_host_validation_without_gpu():
                          scale=0.5, dtype="bf16")
     assert dsa.lib.dsa_sparse_attn_fwd(ctypes.byref(bf), 16, 16, 16, 16, 16, 16, None, None) == \
         dsa.DSA_ERR_UNSUPPORTED
+
+
+def test_backward_workspace_sizes():
+    # bf16 tensor-core backward: P and scale*dS as bf16 hi/lo pairs
+    # [rows*128][k] plus D [rows*128] fp32; the KL pass: head-summed P and dI
+    # [rows][k] plus the indexer logits [rows][64][k], fp32
+    dsa = _lib()
+    rows, k = 24, 2048
+    p = dsa.make_params(B=1, S_q=rows, S_k=16384, H=128, d_qk=576, d_v=512, H_I=64, d_I=128,
+                        topk=k, scale=0.5, dtype="bf16")
+    rh = rows * 128
+    assert dsa.workspace_size(p, dsa.DSA_CALL_ATTN_BWD) == 4 * rh * k * 2 + rh * 4 + 256
+    assert dsa.workspace_size(p, dsa.DSA_CALL_KL_BWD) == 2 * rows * k * 4 + rows * 64 * k * 4 + 256
+    # a k that is not a multiple of 8 has no tensor-core backward
+    odd = dsa.make_params(B=1, S_q=rows, S_k=16384, H=128, d_qk=576, d_v=512, H_I=64, d_I=128,
+                          topk=2047, scale=0.5, dtype="bf16")
+    assert dsa.workspace_size(odd, dsa.DSA_CALL_ATTN_BWD) == 0
+    assert dsa.lib.dsa_sparse_attn_bwd(ctypes.byref(odd), 16, 16, 16, 16, 16, 16, 16, 16, 16, 16,
+                                       None) == dsa.DSA_ERR_UNSUPPORTED
+    # the tensor-core backward needs its workspace
+    assert dsa.lib.dsa_sparse_attn_bwd(ctypes.byref(p), 16, 16, 16, 16, 16, 16, 16, 16, 16, None,
+                                       None) == dsa.DSA_ERR_WORKSPACE

@@ -1,0 +1,86 @@
+"""bf16 tensor-core backward (sparse attention dQ / dKV and the indexer KL
+loss gradients) at the DeepSeek-V3.2 head shapes against the fp64 oracle.
+
+Both sides take the same forward results (the oracle's O rounded to bf16,
+its softmax max / sum rounded to fp32) and the same index sets, so the
+backward is checked on its own."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import DEV, bf16_close, lib, np64, params
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_case(wl, rows):
+    """Oracle forward on `rows` (global positions) of workload `wl`, then the
+    backward on both sides.  The q-side inputs are drawn for len(rows) rows."""
+    n, S, k = len(rows), wl["S"], wl["topk"]
+    x = synth.make_inputs(wl, with_dout=True, S_q=n)
+    pos = oracle.positions(1, n, q_row_index=np.asarray(rows))
+    sc = oracle.indexer_scores(x["q_I"], x["k_I"], x["w"], pos)
+    idx = oracle.topk_select(sc, pos, k)
+    rng = np.random.default_rng(3)
+    for r in range(0, n, 5):                 # shuffled slot order and -1 holes
+        row = idx[0, r].copy()
+        rng.shuffle(row)
+        idx[0, r] = row
+    O, m, l = oracle.sparse_attn_fwd(x["q"], x["kv"], idx, wl["scale"], wl["d_v"])
+    O16 = torch.as_tensor(O).to(torch.bfloat16)
+    m32 = torch.as_tensor(m).float()
+    l32 = torch.as_tensor(l).float()
+
+    dsa = lib()
+    p = params(dsa, wl, S_q=n)
+    g = {nm: v.to(DEV) for nm, v in x.items()}
+    gidx = torch.as_tensor(idx, device=DEV)
+    dq = torch.empty(1, n, wl["H"], wl["d_qk"], dtype=torch.bfloat16, device=DEV)
+    dkv = torch.zeros(1, S, wl["d_qk"], device=DEV)
+    ws = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_ATTN_BWD), dtype=torch.uint8, device=DEV)
+    dsa.sparse_attn_bwd(p, g["q"], g["kv"], gidx, O16.to(DEV), g["dO"], m32.to(DEV), l32.to(DEV),
+                        dq, dkv, ws)
+    loss = torch.zeros(1, device=DEV)
+    dqI = torch.empty(1, n, wl["H_I"], wl["d_I"], dtype=torch.bfloat16, device=DEV)
+    dkI = torch.zeros(1, S, wl["d_I"], device=DEV)
+    dw = torch.empty(1, n, wl["H_I"], device=DEV)
+    ws2 = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_KL_BWD), dtype=torch.uint8, device=DEV)
+    dsa.indexer_kl_loss_bwd(p, g["q"], g["kv"], g["q_I"], g["k_I"], g["w"], gidx, m32.to(DEV),
+                            l32.to(DEV), loss, dqI, dkI, dw, ws2)
+    torch.cuda.synchronize()
+    assert dsa.get_status() == 0
+
+    Od = O16.double().numpy()
+    dq_r, dkv_r = oracle.sparse_attn_bwd(x["q"], x["kv"], idx, Od, x["dO"], m32.double().numpy(),
+                                         l32.double().numpy(), wl["scale"], wl["d_v"])
+    kl_r = oracle.indexer_kl_loss(x["q"], x["kv"], idx, m32.double().numpy(),
+                                  l32.double().numpy(), wl["scale"], x["q_I"], x["k_I"], x["w"])
+    return dict(dq=(np64(dq), dq_r), dkv=(np64(dkv), dkv_r), loss=(float(loss), kl_r[0]),
+                dqI=(np64(dqI), kl_r[1]), dkI=(np64(dkI), kl_r[2]), dw=(np64(dw), kl_r[3]))
+
+
+def _check(res):
+    for key in ("dq", "dkv", "dqI", "dkI", "dw"):
+        got, ref = res[key]
+        ok, ma, mr = bf16_close(got, ref)
+        assert ok, (key, ma, mr)
+    got, ref = res["loss"]
+    assert abs(got - ref) <= 1e-3 * abs(ref), (got, ref)
+
+
+def test_backward_small_ragged():
+    # S = 448, k = 200: partial key tiles, rows with fewer than k causal keys
+    wl = dict(synth.v32(448, "dsv32_S448"), topk=200)
+    _check(_run_case(wl, list(range(448))))
+
+
+def test_backward_train_shape_sampled_rows():
+    # S = 16384, top-2048 (the training configuration): a shard of sampled
+    # query rows against the full key side; dKV / dk_I sum over that shard
+    wl = synth.WORKLOADS["dsv32_S16384_train"]
+    S = wl["S"]
+    rows = sorted(set([0, 1, 2047, 2048, 2049, 8191, S - 2, S - 1] +
+                      np.random.default_rng(5).integers(0, S, 8).tolist()))
+    _check(_run_case(wl, rows))
