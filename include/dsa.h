@@ -156,6 +156,13 @@ int dsa_sparse_attn_fwd(const dsa_params *p, const void *q, const void *kv, cons
  *       zeroes it (or passes partial sums of other shards).
  *   workspace: dsa_workspace_size(p, DSA_CALL_ATTN_BWD) bytes (the fp32 path
  *       accumulates dkv in fp64 there first; NULL allowed when the size is 0).
+ *   bf16 path: DeepSeek head shapes only (H 128, d_qk 576, d_v 512) with
+ *       topk <= 2048 and topk % 8 == 0, else DSA_ERR_UNSUPPORTED; q, kv, out,
+ *       dout, dq, dkv and the workspace 16-byte aligned.  The workspace holds
+ *       P and scale*dS for every (row, head, slot) as bf16 hi/lo pairs plus
+ *       D, i.e. 1024 * rows * topk + 512 * rows + 256 bytes (34 GB at
+ *       rows = 16384, topk = 2048); it must stay untouched until the call's
+ *       kernels have finished on `stream`.
  */
 int dsa_sparse_attn_bwd(const dsa_params *p, const void *q, const void *kv, const int32_t *idx,
                         const void *out, const void *dout, const float *softmax_max,
@@ -174,6 +181,11 @@ int dsa_sparse_attn_bwd(const dsa_params *p, const void *q, const void *kv, cons
  *   dk_I [B, S_k, d_I] fp32 ACCUMULATED with atomics; caller zeroes.
  *   workspace: dsa_workspace_size(p, DSA_CALL_KL_BWD) bytes (fp32 path: fp64
  *       accumulation of dk_I; NULL allowed when the size is 0).
+ *   bf16 path: the attention shapes of dsa_sparse_attn_bwd plus H_I 64,
+ *       d_I 128, else DSA_ERR_UNSUPPORTED; q, kv, k_I, dk_I and the workspace
+ *       16-byte aligned, dq_I 4-byte aligned.  The workspace holds the
+ *       head-summed probabilities, dI and the indexer logits S, all fp32:
+ *       8 * rows * topk + 256 * rows * topk + 256 bytes.
  */
 int dsa_indexer_kl_loss_bwd(const dsa_params *p, const void *q, const void *kv, const void *q_I,
                             const void *k_I, const void *w, const int32_t *idx,

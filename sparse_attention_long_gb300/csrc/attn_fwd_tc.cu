@@ -16,9 +16,10 @@
 //   2. computes the partial logits S_c = Q_c K_c^T (M=128 heads, N=64, K=288)
 //      into one of three TMEM logit buffers,
 //   3. swaps S_c with its peer through distributed shared memory (st.async,
-//      completing on the peer's mbarrier) and forms S = S_0 + S_1 (the same
-//      fp32 sum in both CTAs, so both derive the same softmax state and the
-//      same P without a second exchange),
+//      completing on the peer's mbarrier; four exchange warps send each block
+//      as soon as its logits are in TMEM, independently of the softmax) and
+//      forms S = S_0 + S_1 (the same fp32 sum in both CTAs, so both derive the
+//      same softmax state and the same P without a second exchange),
 //   4. runs the fp32 online softmax (one thread per head, exp2 domain; the
 //      running max used for P only moves when it grows by > 2^8, so the O
 //      rescale in TMEM is rare) and writes P as bf16 back over the logits in
@@ -30,8 +31,9 @@
 // in shared memory once, so no global load sits on the per-block path.
 //
 // Roles per CTA: warp 0 = TMEM owner + MMA issuer, warps 1..4 = kv gather (warp 1
-// also TMA-loads the query half), warps 5..12 = softmax / exchange / epilogue:
-// two warps per TMEM lane quadrant, thread = (head, half of the block's keys).
+// also TMA-loads the query half), warps 5..8 = logit exchange (thread = head),
+// warps 9..16 = softmax / epilogue: two warps per TMEM lane quadrant, thread =
+// (head, half of the block's keys).
 #include <math.h>
 
 #include "dsa_common.cuh"
@@ -53,8 +55,10 @@ constexpr int kKVRope = kBKey * 64;               // 4 KB
 constexpr int kKVStage = 4 * kKVChunk + kKVRope;  // 36 KB
 constexpr int kSoftWarps = 8;                     // two per TMEM lane quadrant
 constexpr int kGatherWarps = 4;
-constexpr int kWarpMMA = 0, kWarpGather0 = 1, kWarpSoft0 = kWarpGather0 + kGatherWarps;
-constexpr int kThreads = 32 * (1 + kGatherWarps + kSoftWarps);
+constexpr int kXWarps = 4;                        // one per TMEM lane quadrant
+constexpr int kWarpMMA = 0, kWarpGather0 = 1, kWarpX0 = kWarpGather0 + kGatherWarps,
+              kWarpSoft0 = kWarpX0 + kXWarps;
+constexpr int kThreads = 32 * (1 + kGatherWarps + kXWarps + kSoftWarps);
 constexpr int kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256;        // O: [0,256)  logits/P: 256 + 64*b
 constexpr uint32_t kIdescS = idesc_bf16(128, kBKey, false, false);
@@ -71,11 +75,12 @@ struct __align__(1024) Smem {
   int32_t idx[kMaxTopk];                          // the token's index row (-1 = skip)
   unsigned long long mask[kMaxBlk];               // per 64-slot block: valid slots
   uint64_t q_full, kv_full[kStages], kv_empty[kStages], s_full[kSBuf], s_free[kSBuf],
-      p_full[kSBuf], x_full, x_free, mma_done;
+      s_read[kSBuf], p_full[kSBuf], x_full, x_free, mma_done;
   uint32_t tmem_base;
   int abort;
   int last;
   int bad;
+  uint32_t sink;                                  // target of the load-completion guard
 };
 static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory budget");
 
@@ -122,6 +127,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kSBuf; ++i) {
       mbar_init(smem_u32(&sm.s_full[i]), 1);
       mbar_init(smem_u32(&sm.s_free[i]), 1);
+      mbar_init(smem_u32(&sm.s_read[i]), kXWarps);  // the exchange warps hold the logits
       mbar_init(smem_u32(&sm.p_full[i]), kSoftWarps * 32);
     }
     mbar_init(smem_u32(&sm.x_full), 1);            // local arm + the peer's st.async bytes
@@ -172,7 +178,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  if (warp >= kWarpGather0 && warp < kWarpSoft0) {
+  if (warp >= kWarpGather0 && warp < kWarpX0) {
     // ------------------------------- kv gather -------------------------------
     // warp gw owns keys gw, gw+4, ..., gw+60 of every block.  Latent half: one
     // warp-wide 16-byte load per key (lane = 16-byte chunk of the 512 bytes);
@@ -291,51 +297,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mma_commit(smem_u32(&sm.mma_done));
       mbar_wait(smem_u32(&sm.mma_done), 0, c, abort_flag);
     }
+  } else if (warp < kWarpSoft0) {
+    // ------------------------------ logit exchange ------------------------------
+    // Thread = head: as soon as block j's partial logits are in TMEM, copy all
+    // 64 of them into the peer's exchange buffer (once the peer has consumed
+    // block j-1 from it).  Layout there: [16 chunks of 4 keys][head][4] fp32.
+    const int h = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t x_remote = mapa_shared(smem_u32(sm.x), peer);
+    const uint32_t xfull_remote = mapa_shared(smem_u32(&sm.x_full), peer);
+    for (int j = 0; j < nblk; ++j) {
+      const int sb = j % kSBuf;
+      if (!mbar_wait_warp(smem_u32(&sm.s_full[sb]), (j / kSBuf) & 1, c, abort_flag)) break;
+      tc_fence_after();
+      uint32_t u[2][32];
+      tmem_ld32(tmem + lane_off + kColS + sb * kBKey, u[0]);
+      tmem_ld32(tmem + lane_off + kColS + sb * kBKey + 32, u[1]);
+      tmem_ld_wait(u[0]);
+      tmem_ld_also(u[1]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.s_read[sb]));  // P may now overwrite them
+      if (j > 0 && !mbar_wait_warp<true>(smem_u32(&sm.x_free), (j - 1) & 1, c, abort_flag)) break;
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch)
+        st_async_v4(x_remote + ((ch * kH + h) << 4), u[ch >> 3][4 * (ch & 7)],
+                    u[ch >> 3][4 * (ch & 7) + 1], u[ch >> 3][4 * (ch & 7) + 2],
+                    u[ch >> 3][4 * (ch & 7) + 3], xfull_remote);
+    }
   } else {
-    // ----------------------- softmax / exchange / epilogue --------------------
+    // --------------------------- softmax / epilogue ---------------------------
     const int sw = warp - kWarpSoft0;                    // 0..7
     const int hf = sw >> 2;                              // key half of each block
     const int quad = warp & 3;
     const int h = quad * 32 + lane;                      // this thread's head (TMEM lane)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t xfull = smem_u32(&sm.x_full);
-    const uint32_t x_remote = mapa_shared(smem_u32(sm.x), peer);
-    const uint32_t xfull_remote = mapa_shared(xfull, peer);
     const uint32_t xfree_remote = mapa_shared(smem_u32(&sm.x_free), peer);
     const float sl2e = s.scale * kLog2e;
     const bool armer = (sw == 0 && lane == 0);
     float m_run = -INFINITY, m_true = -INFINITY, l_run = 0.f;
-    // Software-pipelined: block j+1's partial logits go out to the peer before
-    // block j's softmax arithmetic, so the exchange latency overlaps it.
     // A failed (timed-out) wait turns the rest of this warp's work into no-ops,
     // but every softmax warp still executes the same named barriers.
     bool ok = true;
-    uint32_t u[32];  // partial logits of the block being sent / held
-    auto fetch_and_send = [&](int jb) {
-      const int sbb = jb % kSBuf;
-      ok = ok && mbar_wait_warp(smem_u32(&sm.s_full[sbb]), (jb / kSBuf) & 1, c, abort_flag);
-      if (ok) {
-        tc_fence_after();
-        tmem_ld32(tmem + lane_off + kColS + sbb * kBKey + 32 * hf, u);
-        tmem_ld_wait();
-      }
-      // the peer has consumed block jb-1 from its exchange buffer
-      if (jb > 0) ok = ok && mbar_wait_warp<true>(smem_u32(&sm.x_free), (jb - 1) & 1, c, abort_flag);
-      if (ok) {
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          st_async_v4(x_remote + (((8 * hf + ch) * kH + h) << 4), u[4 * ch], u[4 * ch + 1],
-                      u[4 * ch + 2], u[4 * ch + 3], xfull_remote);
-      }
-    };
-    if (nblk > 0) {
-      if (armer) mbar_arrive_expect_tx(xfull, kH * kBKey * 4);  // phase 0 of x_full
-      fetch_and_send(0);
-    }
+    if (nblk > 0 && armer) mbar_arrive_expect_tx(xfull, kH * kBKey * 4);  // phase 0 of x_full
     for (int j = 0; j < nblk; ++j) {
       const int sb = j % kSBuf;
       const uint32_t vmask = (uint32_t)(sm.mask[j] >> (32 * hf));
       const uint32_t sbuf = tmem + lane_off + kColS + sb * kBKey;
+      ok = ok && mbar_wait_warp(smem_u32(&sm.s_full[sb]), (j / kSBuf) & 1, c, abort_flag);
+      uint32_t u[32];
+      if (ok) {
+        tc_fence_after();
+        tmem_ld32(sbuf + 32 * hf, u);
+        tmem_ld_wait(u);
+      }
       ok = ok && mbar_wait_warp<true>(xfull, j & 1, c, abort_flag);
       float v[32];
       if (ok) {
@@ -347,18 +363,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           v[4 * ch + 2] = __uint_as_float(u[4 * ch + 2]) + pr.z;
           v[4 * ch + 3] = __uint_as_float(u[4 * ch + 3]) + pr.w;
         }
-        // The arrive below is relaxed, so nothing but issue order keeps it behind
-        // the exchange-buffer loads: fold every loaded value into `dep` (real
-        // instructions that must wait for the load data) and make the arrive
-        // take it as an operand.
+        // Release the buffer to the peer only once every lane's loads have
+        // landed.  The arrive is relaxed (it orders nothing by itself), so each
+        // lane first feeds all its loaded values into a compare that guards a
+        // (practically never taken) shared store: the compare cannot issue
+        // before the load data is in registers, the store keeps it from being
+        // optimised away, and __syncwarp keeps lane 0's arrive behind every
+        // lane's compare.  Nobody waits for the last block's release, and a
+        // remote arrive still in flight when the pair exits could land on the
+        // barrier of the next CTA placed on the peer's SM, so it is skipped.
         uint32_t dep = 0;
 #pragma unroll
         for (int i = 0; i < 32; ++i) dep ^= __float_as_uint(v[i]);
+        if (dep == 0x9e3779b9u) sm.sink = dep;
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote_relaxed_after(xfree_remote, dep);
+        if (lane == 0 && j + 1 < nblk) mbar_arrive_remote_relaxed(xfree_remote);
         if (armer && j + 1 < nblk) mbar_arrive_expect_tx(xfull, kH * kBKey * 4);  // phase j+1
       }
-      if (j + 1 < nblk) fetch_and_send(j + 1);
       float bm = -INFINITY;
       if (ok) {
         if (vmask != 0xffffffffu) {
@@ -392,10 +413,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int cc = 128 * hf; cc < 128 * hf + 128; cc += 32) {
             uint32_t o[32];
             tmem_ld32(tmem + lane_off + kColO + cc, o);
-            tmem_ld_wait();
+            tmem_ld_wait(o);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
             tmem_st32(tmem + lane_off + kColO + cc, o);
+            tmem_st_wait();  // the source registers are reused by the next load
           }
         }
         l_run *= alpha;
@@ -410,6 +432,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         l_run += pa + pb;
         pk[i] = pack_bf16x2(pa, pb);
       }
+      // P goes over logits the exchange warps read: wait until they hold them
+      ok = mbar_wait_warp(smem_u32(&sm.s_read[sb]), (j / kSBuf) & 1, c, abort_flag);
+      if (!ok) continue;
+      tc_fence_after();
       tmem_st16(sbuf + 16 * hf, pk);  // P (bf16 pairs) over the logits of this block
       tmem_st_wait();
       tc_fence_before();
@@ -432,7 +458,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t o[32];
       if (__all_sync(0xffffffffu, have)) {
         tmem_ld32(tmem + lane_off + kColO + c0 + cc, o);
-        tmem_ld_wait();
+        tmem_ld_wait(o);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = 0u;

@@ -230,7 +230,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
       if (have) {
         tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + cc, sv);
         if (kGrad) tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + 128 + cc, dv);
-        tmem_ld_wait();
+        tmem_ld_wait(sv);
+        if (kGrad) tmem_ld_also(dv);
       }
       const uint32_t vm = sm.mask[cc >> 5];
       float p[32];
@@ -421,7 +422,7 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t v[32];
       if (have) {
         tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + cc, v);
-        tmem_ld_wait();
+        tmem_ld_wait(v);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0u;
@@ -564,7 +565,7 @@ __global__ void __launch_bounds__(128, 1)
       uint32_t v[32];
       if (have) {
         tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + cc, v);
-        tmem_ld_wait();
+        tmem_ld_wait(v);
         if (id >= 0) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4)

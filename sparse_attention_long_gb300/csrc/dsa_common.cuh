@@ -86,12 +86,10 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
 }
-// Remote arrive with no ordering of earlier memory operations; `dep` (unused
-// by the instruction) pins it after the computation of `dep` in issue order.
-__device__ __forceinline__ void mbar_arrive_remote_relaxed_after(uint32_t cluster_bar,
-                                                                 uint32_t dep) {
-  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar),
-               "r"(dep)
+// Remote arrive that orders no earlier memory operation: the caller must make
+// sure by other means that what it releases is no longer being read.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
 }
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
@@ -242,8 +240,22 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
 }
-__device__ __forceinline__ void tmem_ld_wait() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+// tcgen05.ld writes its destination registers asynchronously: they hold the
+// data only after tcgen05.wait::ld.  The compiler sees them as defined by the
+// load statement, so plain arithmetic on them could be scheduled before the
+// wait.  The waits below therefore take the destination arrays as in/out
+// operands: every use is data-dependent on the wait.
+#define DSA_RW8(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), \
+                   "+r"(r[i + 4]), "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : DSA_RW8(0), DSA_RW8(8), DSA_RW8(16), DSA_RW8(24)
+               :
+               : "memory");
+}
+// after a tmem_ld_wait: ties one more destination array to that wait
+__device__ __forceinline__ void tmem_ld_also(uint32_t (&r)[32]) {
+  asm volatile("" : DSA_RW8(0), DSA_RW8(8), DSA_RW8(16), DSA_RW8(24) : : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");

@@ -176,7 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v0[32], v1[32];
         tmem_ld32(ta, v0);
         tmem_ld32(ta + 32, v1);
-        tmem_ld_wait();
+        tmem_ld_wait(v0);
+        tmem_ld_also(v1);
         const float* wj = sm.w[j];
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
