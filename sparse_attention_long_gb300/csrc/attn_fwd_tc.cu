@@ -15,15 +15,16 @@
 //      key's contiguous 512-byte latent half, so every load is coalesced),
 //   2. computes the partial logits S_c = Q_c K_c^T (M=128 heads, N=64, K=288)
 //      into one of three TMEM logit buffers,
-//   3. swaps S_c with its peer through distributed shared memory (st.async,
-//      completing on the peer's mbarrier; four exchange warps send each block
-//      as soon as its logits are in TMEM, independently of the softmax) and
-//      forms S = S_0 + S_1 (the same fp32 sum in both CTAs, so both derive the
-//      same softmax state and the same P without a second exchange),
-//   4. runs the fp32 online softmax (one thread per head, exp2 domain; the
-//      running max used for P only moves when it grows by > 2^8, so the O
-//      rescale in TMEM is rare) and writes P as bf16 back over the logits in
-//      TMEM,
+//   3. swaps S_c with its peer through distributed shared memory: four
+//      exchange warps send each block as soon as its logits are in TMEM
+//      (st.async, completing on the peer's mbarrier), add the peer's partial
+//      when it lands (the same fp32 sum in both CTAs, so both derive the same
+//      softmax state and the same P without a second exchange), release the
+//      buffer at once and write the full logits back to TMEM,
+//   4. runs the fp32 online softmax (one thread per head over all 64 keys of
+//      the block, exp2 domain; the running max used for P only moves when it
+//      grows by > 2^8, so the O rescale in TMEM is rare) and writes P as bf16
+//      back over the logits in TMEM,
 //   5. accumulates O_c += P V_c (M=128, N=256, K=64) with P read from TMEM and
 //      V_c from the same gathered tile as an MN-major operand.
 // No multiply is duplicated across the pair; only the exp of the shared
@@ -31,9 +32,8 @@
 // in shared memory once, so no global load sits on the per-block path.
 //
 // Roles per CTA: warp 0 = TMEM owner + MMA issuer, warps 1..4 = kv gather (warp 1
-// also TMA-loads the query half), warps 5..8 = logit exchange (thread = head),
-// warps 9..16 = softmax / epilogue: two warps per TMEM lane quadrant, thread =
-// (head, half of the block's keys).
+// also TMA-loads the query half), warps 5..8 = logit exchange and sum, warps
+// 9..12 = softmax / epilogue (one warp per TMEM lane quadrant, thread = head).
 #include <math.h>
 
 #include "dsa_common.cuh"
@@ -53,7 +53,7 @@ constexpr int kQBytes = 4 * kQChunk + kQRope;     // 72 KB
 constexpr int kKVChunk = kBKey * 128;             // 8 KB
 constexpr int kKVRope = kBKey * 64;               // 4 KB
 constexpr int kKVStage = 4 * kKVChunk + kKVRope;  // 36 KB
-constexpr int kSoftWarps = 8;                     // two per TMEM lane quadrant
+constexpr int kSoftWarps = 4;                     // one per TMEM lane quadrant
 constexpr int kGatherWarps = 4;
 constexpr int kXWarps = 4;                        // one per TMEM lane quadrant
 constexpr int kWarpMMA = 0, kWarpGather0 = 1, kWarpX0 = kWarpGather0 + kGatherWarps,
@@ -71,11 +71,10 @@ struct __align__(1024) Smem {
   uint8_t q[kQBytes];
   uint8_t kv[kStages][kKVStage];
   float x[kH * kBKey];                            // peer's partial logits [16 x 4-key chunk][head][4]
-  float red[2][2][kH];                            // per-block max of each key half (double buffered)
   int32_t idx[kMaxTopk];                          // the token's index row (-1 = skip)
   unsigned long long mask[kMaxBlk];               // per 64-slot block: valid slots
   uint64_t q_full, kv_full[kStages], kv_empty[kStages], s_full[kSBuf], s_free[kSBuf],
-      s_read[kSBuf], p_full[kSBuf], x_full, x_free, mma_done;
+      c_full[kSBuf], p_full[kSBuf], x_full, x_free, mma_done;
   uint32_t tmem_base;
   int abort;
   int last;
@@ -127,11 +126,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kSBuf; ++i) {
       mbar_init(smem_u32(&sm.s_full[i]), 1);
       mbar_init(smem_u32(&sm.s_free[i]), 1);
-      mbar_init(smem_u32(&sm.s_read[i]), kXWarps);  // the exchange warps hold the logits
+      mbar_init(smem_u32(&sm.c_full[i]), kXWarps);  // full logits back in TMEM
       mbar_init(smem_u32(&sm.p_full[i]), kSoftWarps * 32);
     }
     mbar_init(smem_u32(&sm.x_full), 1);            // local arm + the peer's st.async bytes
-    mbar_init(smem_u32(&sm.x_free), kSoftWarps);   // one arrive per peer softmax warp
+    mbar_init(smem_u32(&sm.x_free), kXWarps);      // one arrive per peer exchange warp
     mbar_init(smem_u32(&sm.mma_done), 1);
     sm.abort = 0;
     sm.last = -1;
@@ -298,119 +297,116 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_wait(smem_u32(&sm.mma_done), 0, c, abort_flag);
     }
   } else if (warp < kWarpSoft0) {
-    // ------------------------------ logit exchange ------------------------------
-    // Thread = head: as soon as block j's partial logits are in TMEM, copy all
+    // ------------------------- logit exchange and sum -------------------------
+    // Thread = head.  As soon as block j's partial logits are in TMEM, copy all
     // 64 of them into the peer's exchange buffer (once the peer has consumed
-    // block j-1 from it).  Layout there: [16 chunks of 4 keys][head][4] fp32.
+    // block j-1 from it), then wait for the peer's partial, add it, release the
+    // buffer at once and write the full logits back over the partial in TMEM.
+    // Exchange layout: [16 chunks of 4 keys][head][4] fp32.
     const int h = (warp & 3) * 32 + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t xfull = smem_u32(&sm.x_full);
     const uint32_t x_remote = mapa_shared(smem_u32(sm.x), peer);
-    const uint32_t xfull_remote = mapa_shared(smem_u32(&sm.x_full), peer);
+    const uint32_t xfull_remote = mapa_shared(xfull, peer);
+    const uint32_t xfree_remote = mapa_shared(smem_u32(&sm.x_free), peer);
+    const bool armer = (warp == kWarpX0 && lane == 0);
+    if (nblk > 0 && armer) mbar_arrive_expect_tx(xfull, kH * kBKey * 4);  // block 0
     for (int j = 0; j < nblk; ++j) {
       const int sb = j % kSBuf;
+      const uint32_t sbuf = tmem + lane_off + kColS + sb * kBKey;
       if (!mbar_wait_warp(smem_u32(&sm.s_full[sb]), (j / kSBuf) & 1, c, abort_flag)) break;
       tc_fence_after();
       uint32_t u[2][32];
-      tmem_ld32(tmem + lane_off + kColS + sb * kBKey, u[0]);
-      tmem_ld32(tmem + lane_off + kColS + sb * kBKey + 32, u[1]);
+      tmem_ld32(sbuf, u[0]);
+      tmem_ld32(sbuf + 32, u[1]);
       tmem_ld_wait(u[0]);
       tmem_ld_also(u[1]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.s_read[sb]));  // P may now overwrite them
       if (j > 0 && !mbar_wait_warp<true>(smem_u32(&sm.x_free), (j - 1) & 1, c, abort_flag)) break;
 #pragma unroll
       for (int ch = 0; ch < 16; ++ch)
         st_async_v4(x_remote + ((ch * kH + h) << 4), u[ch >> 3][4 * (ch & 7)],
                     u[ch >> 3][4 * (ch & 7) + 1], u[ch >> 3][4 * (ch & 7) + 2],
                     u[ch >> 3][4 * (ch & 7) + 3], xfull_remote);
+      if (!mbar_wait_warp<true>(xfull, j & 1, c, abort_flag)) break;
+      uint32_t dep = 0;
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        const float4 pr = *reinterpret_cast<const float4*>(sm.x + (ch * kH + h) * 4);
+        uint32_t* w = &u[ch >> 3][4 * (ch & 7)];
+        w[0] = __float_as_uint(__uint_as_float(w[0]) + pr.x);
+        w[1] = __float_as_uint(__uint_as_float(w[1]) + pr.y);
+        w[2] = __float_as_uint(__uint_as_float(w[2]) + pr.z);
+        w[3] = __float_as_uint(__uint_as_float(w[3]) + pr.w);
+        dep ^= __float_as_uint(pr.x) ^ __float_as_uint(pr.y) ^ __float_as_uint(pr.z) ^
+               __float_as_uint(pr.w);
+      }
+      // Release the buffer to the peer only once every lane's loads have
+      // landed.  The arrive is relaxed (it orders nothing by itself), so each
+      // lane first feeds all its loaded values into a compare that guards a
+      // (practically never taken) shared store: the compare cannot issue
+      // before the load data is in registers, the store keeps it from being
+      // optimised away, and __syncwarp keeps lane 0's arrive behind every
+      // lane's compare.  Nobody waits for the last block's release, and a
+      // remote arrive still in flight when the pair exits could land on the
+      // barrier of the next CTA placed on the peer's SM, so it is skipped.
+      if (dep == 0x9e3779b9u) sm.sink = dep;
+      __syncwarp();
+      if (lane == 0 && j + 1 < nblk) mbar_arrive_remote_relaxed(xfree_remote);
+      if (armer && j + 1 < nblk) mbar_arrive_expect_tx(xfull, kH * kBKey * 4);  // block j+1
+      tmem_st32(sbuf, u[0]);
+      tmem_st32(sbuf + 32, u[1]);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.c_full[sb]));
     }
   } else {
     // --------------------------- softmax / epilogue ---------------------------
-    const int sw = warp - kWarpSoft0;                    // 0..7
-    const int hf = sw >> 2;                              // key half of each block
+    // Thread = head, all 64 keys of each block.
     const int quad = warp & 3;
     const int h = quad * 32 + lane;                      // this thread's head (TMEM lane)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t xfull = smem_u32(&sm.x_full);
-    const uint32_t xfree_remote = mapa_shared(smem_u32(&sm.x_free), peer);
     const float sl2e = s.scale * kLog2e;
-    const bool armer = (sw == 0 && lane == 0);
     float m_run = -INFINITY, m_true = -INFINITY, l_run = 0.f;
-    // A failed (timed-out) wait turns the rest of this warp's work into no-ops,
-    // but every softmax warp still executes the same named barriers.
+    // A failed (timed-out) wait turns the rest of this warp's work into no-ops.
     bool ok = true;
-    if (nblk > 0 && armer) mbar_arrive_expect_tx(xfull, kH * kBKey * 4);  // phase 0 of x_full
-    for (int j = 0; j < nblk; ++j) {
+    for (int j = 0; ok && j < nblk; ++j) {
       const int sb = j % kSBuf;
-      const uint32_t vmask = (uint32_t)(sm.mask[j] >> (32 * hf));
       const uint32_t sbuf = tmem + lane_off + kColS + sb * kBKey;
-      ok = ok && mbar_wait_warp(smem_u32(&sm.s_full[sb]), (j / kSBuf) & 1, c, abort_flag);
-      uint32_t u[32];
-      if (ok) {
-        tc_fence_after();
-        tmem_ld32(sbuf + 32 * hf, u);
-        tmem_ld_wait(u);
-      }
-      ok = ok && mbar_wait_warp<true>(xfull, j & 1, c, abort_flag);
-      float v[32];
-      if (ok) {
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const float4 pr = *reinterpret_cast<const float4*>(sm.x + ((8 * hf + ch) * kH + h) * 4);
-          v[4 * ch + 0] = __uint_as_float(u[4 * ch + 0]) + pr.x;
-          v[4 * ch + 1] = __uint_as_float(u[4 * ch + 1]) + pr.y;
-          v[4 * ch + 2] = __uint_as_float(u[4 * ch + 2]) + pr.z;
-          v[4 * ch + 3] = __uint_as_float(u[4 * ch + 3]) + pr.w;
-        }
-        // Release the buffer to the peer only once every lane's loads have
-        // landed.  The arrive is relaxed (it orders nothing by itself), so each
-        // lane first feeds all its loaded values into a compare that guards a
-        // (practically never taken) shared store: the compare cannot issue
-        // before the load data is in registers, the store keeps it from being
-        // optimised away, and __syncwarp keeps lane 0's arrive behind every
-        // lane's compare.  Nobody waits for the last block's release, and a
-        // remote arrive still in flight when the pair exits could land on the
-        // barrier of the next CTA placed on the peer's SM, so it is skipped.
-        uint32_t dep = 0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) dep ^= __float_as_uint(v[i]);
-        if (dep == 0x9e3779b9u) sm.sink = dep;
-        __syncwarp();
-        if (lane == 0 && j + 1 < nblk) mbar_arrive_remote_relaxed(xfree_remote);
-        if (armer && j + 1 < nblk) mbar_arrive_expect_tx(xfull, kH * kBKey * 4);  // phase j+1
-      }
+      ok = mbar_wait_warp(smem_u32(&sm.c_full[sb]), (j / kSBuf) & 1, c, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t v[2][32];
+      tmem_ld32(sbuf, v[0]);
+      tmem_ld32(sbuf + 32, v[1]);
+      tmem_ld_wait(v[0]);
+      tmem_ld_also(v[1]);
+      const unsigned long long vmask = sm.mask[j];
       float bm = -INFINITY;
-      if (ok) {
-        if (vmask != 0xffffffffu) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (((vmask >> i) & 1u) == 0) v[i] = -INFINITY;
-        }
-        bm = v[0];
-#pragma unroll
-        for (int i = 1; i < 32; ++i) bm = fmaxf(bm, v[i]);
+      for (int i = 0; i < 64; ++i) {
+        float x = __uint_as_float(v[i >> 5][i & 31]);
+        if (((vmask >> i) & 1ull) == 0) x = -INFINITY;
+        v[i >> 5][i & 31] = __float_as_uint(x);
+        bm = fmaxf(bm, x);
       }
-      sm.red[j & 1][hf][h] = bm;
-      named_bar_sync(1, kSoftWarps * 32);  // both halves loaded their logits; maxima visible
-      if (!ok) continue;
-      bm = fmaxf(bm, sm.red[j & 1][hf ^ 1][h]) * sl2e;  // block max, log2 units (sl2e > 0)
+      bm *= sl2e;                                        // block max, log2 units (sl2e > 0)
       m_true = fmaxf(m_true, bm);
       const bool need = bm > m_run + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need)) {  // same vote in both halves (same maxima)
+      if (__any_sync(0xffffffffu, need)) {  // the same vote in both CTAs (same logits)
         const float m_new = fmaxf(m_run, bm);
         const float alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - m_new);
         if (j > 0 && __any_sync(0xffffffffu, m_run != -INFINITY)) {
-          // O must hold PV(j-1) before it is rescaled; each half owns 128 columns.
-          // s_free[b] completes once per PV on buffer b; the phase before the one
-          // awaited is known complete (S(j-1) reused the buffer), so the parity
-          // test is unambiguous, and PVs complete in issue order.
+          // O must hold PV(j-1) before it is rescaled.  s_free[b] completes
+          // once per PV on buffer b; the phase before the one awaited is known
+          // complete (S(j-1) reused the buffer), so the parity test is
+          // unambiguous, and PVs complete in issue order.
           ok = mbar_wait_warp(smem_u32(&sm.s_free[(j - 1) % kSBuf]), ((j - 1) / kSBuf) & 1, c,
                               abort_flag);
-          if (!ok) continue;
+          if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
-          for (int cc = 128 * hf; cc < 128 * hf + 128; cc += 32) {
+          for (int cc = 0; cc < 256; cc += 32) {
             uint32_t o[32];
             tmem_ld32(tmem + lane_off + kColO + cc, o);
             tmem_ld_wait(o);
@@ -424,19 +420,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         m_run = m_new;
       }
       const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-      uint32_t pk[16];
+      uint32_t pk[32];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float pa = ex2(fmaf(v[2 * i], sl2e, -mu));
-        const float pb = ex2(fmaf(v[2 * i + 1], sl2e, -mu));
+      for (int i = 0; i < 32; ++i) {
+        const float pa = ex2(fmaf(__uint_as_float(v[i >> 4][(2 * i) & 31]), sl2e, -mu));
+        const float pb = ex2(fmaf(__uint_as_float(v[i >> 4][(2 * i + 1) & 31]), sl2e, -mu));
         l_run += pa + pb;
         pk[i] = pack_bf16x2(pa, pb);
       }
-      // P goes over logits the exchange warps read: wait until they hold them
-      ok = mbar_wait_warp(smem_u32(&sm.s_read[sb]), (j / kSBuf) & 1, c, abort_flag);
-      if (!ok) continue;
-      tc_fence_after();
-      tmem_st16(sbuf + 16 * hf, pk);  // P (bf16 pairs) over the logits of this block
+      tmem_st32(sbuf, pk);  // P (bf16 pairs) over the first 32 logit columns of the block
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.p_full[sb]));
@@ -447,17 +439,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       have = mbar_wait_warp(smem_u32(&sm.s_free[(nblk - 1) % kSBuf]), ((nblk - 1) / kSBuf) & 1, c,
                             abort_flag);
     tc_fence_after();
-    sm.red[nblk & 1][hf][h] = l_run;  // the buffer the last block's maxima did not use
-    named_bar_sync(1, kSoftWarps * 32);
-    const float l_all = sm.red[nblk & 1][0][h] + sm.red[nblk & 1][1][h];
-    const float inv = (have && l_all > 0.f) ? 1.f / l_all : 0.f;
-    const int c0 = 128 * hf;
-    __nv_bfloat16* orow = out + (row * kH + h) * (long long)kDV + 256 * crank + c0;
+    const float inv = (have && l_run > 0.f) ? 1.f / l_run : 0.f;
+    __nv_bfloat16* orow = out + (row * kH + h) * (long long)kDV + 256 * crank;
 #pragma unroll 1
-    for (int cc = 0; cc < 128; cc += 32) {
+    for (int cc = 0; cc < 256; cc += 32) {
       uint32_t o[32];
       if (__all_sync(0xffffffffu, have)) {
-        tmem_ld32(tmem + lane_off + kColO + c0 + cc, o);
+        tmem_ld32(tmem + lane_off + kColO + cc, o);
         tmem_ld_wait(o);
       } else {
 #pragma unroll
@@ -472,10 +460,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 4; ++i) dst[i] = pk[i];
     }
-    if (crank == 0 && hf == 0) {
+    if (crank == 0) {
       const bool any = have && m_true != -INFINITY;
       mx[row * kH + h] = any ? m_true * kLn2 : -INFINITY;
-      sm_out[row * kH + h] = any ? l_all * ex2(m_run - m_true) : 0.f;
+      sm_out[row * kH + h] = any ? l_run * ex2(m_run - m_true) : 0.f;
     }
   }
   tc_fence_before();
