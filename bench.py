@@ -63,6 +63,91 @@ def algorithmic(wl, pos):
     return f_idx, f_attn, topk_bytes
 
 
+def algorithmic_bwd(wl, pos):
+    """Backward work: attention backward 2*H*(3*d_qk + 2*d_v) flops per selected
+    pair (S and dP recomputed, dQ, dK, dV) and the indexer KL pass
+    (2*H*d_qk + 3*2*H_I*d_I) per selected pair (the probability recompute, the
+    indexer logits, dq_I and dk_I)."""
+    sel = np.minimum(pos.astype(np.float64) + 1.0, wl["topk"]).sum()
+    f_bwd = 2.0 * wl["H"] * (3 * wl["d_qk"] + 2 * wl["d_v"]) * sel
+    f_kl = (2.0 * wl["H"] * wl["d_qk"] + 3 * 2.0 * wl["H_I"] * wl["d_I"]) * sel
+    return f_bwd, f_kl
+
+
+def time_calls(fn, steps, warmup, stream):
+    """Mean ms of fn() over `steps` calls after `warmup`, CUDA events on `stream`."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def backward_stage(dsa, dev, steps, peak_tc):
+    """The training-shape backward (S = 16384, top-2048, all rows): forward once
+    for the indices and softmax statistics, then the attention backward
+    (dq, dkv) and the indexer KL-loss backward, each timed alone."""
+    wl = synth.WORKLOADS["dsv32_S16384_train"]
+    S, k, H = wl["S"], wl["topk"], wl["H"]
+    x = synth.make_inputs(wl, device=dev, with_dout=True)
+    p = dsa.make_params(B=1, S_q=S, S_k=S, H=H, d_qk=wl["d_qk"], d_v=wl["d_v"], H_I=wl["H_I"],
+                        d_I=wl["d_I"], topk=k, scale=wl["scale"], dtype="bf16")
+    ring = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_FORWARD), dtype=torch.uint8, device=dev)
+    idx = torch.empty(1, S, k, dtype=torch.int32, device=dev)
+    out = torch.empty(1, S, H, wl["d_v"], dtype=torch.bfloat16, device=dev)
+    m = torch.empty(1, S, H, device=dev)
+    l = torch.empty_like(m)
+    dq = torch.empty(1, S, H, wl["d_qk"], dtype=torch.bfloat16, device=dev)
+    dkv = torch.zeros(1, S, wl["d_qk"], device=dev)
+    ws_b = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_ATTN_BWD), dtype=torch.uint8, device=dev)
+    loss = torch.zeros(1, device=dev)
+    dq_I = torch.empty(1, S, wl["H_I"], wl["d_I"], dtype=torch.bfloat16, device=dev)
+    dk_I = torch.zeros(1, S, wl["d_I"], device=dev)
+    dw = torch.empty(1, S, wl["H_I"], device=dev)
+    ws_k = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_KL_BWD), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fwd = lambda: dsa.forward(p, x["q_I"], x["k_I"], x["w"], x["q"], x["kv"], idx, out, m, l, ring)
+    bwd = lambda: dsa.sparse_attn_bwd(p, x["q"], x["kv"], idx, out, x["dO"], m, l, dq, dkv, ws_b)
+    kl = lambda: dsa.indexer_kl_loss_bwd(p, x["q"], x["kv"], x["q_I"], x["k_I"], x["w"], idx, m, l,
+                                         loss, dq_I, dk_I, dw, ws_k)
+    t_fwd = time_calls(fwd, steps, 1, stream)
+    t_bwd = time_calls(bwd, steps, 1, stream)
+    t_kl = time_calls(kl, steps, 1, stream)
+    assert dsa.get_status() == 0, "device status after the backward"
+    f_bwd, f_kl = algorithmic_bwd(wl, np.arange(S))
+    return {"workload": wl["name"], "calls_timed": steps,
+            "forward_ms": t_fwd, "attn_bwd_ms": t_bwd, "kl_bwd_ms": t_kl,
+            "attn_bwd_tflops": f_bwd / (t_bwd * 1e-3) / 1e12,
+            "kl_bwd_tflops": f_kl / (t_kl * 1e-3) / 1e12,
+            "attn_bwd_frac": f_bwd / (t_bwd * 1e-3) / 1e12 / peak_tc,
+            "workspace_bytes": {"attn_bwd": ws_b.numel(), "kl_bwd": ws_k.numel()},
+            "note": "outside the timed forward step; dkv / dk_I accumulate over calls"}
+
+
+def topk_stage(dsa, dev, wl, steps, warmup, peaks):
+    """Top-k alone on the last wave of the workload (rows at the end of the
+    sequence, the longest ones) over seeded N(0, 8^2) scores; a profiling aid."""
+    S, k = wl["S"], wl["topk"]
+    R = min(2048, S)
+    p = dsa.make_params(B=1, S_q=R, S_k=S, H=wl["H"], d_qk=wl["d_qk"], d_v=wl["d_v"],
+                        H_I=wl["H_I"], d_I=wl["d_I"], topk=k, scale=wl["scale"], dtype="bf16",
+                        q_row_offset=S - R)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    sc = torch.randn(R, S, device=dev, generator=g) * 8.0
+    idx = torch.empty(R, k, dtype=torch.int32, device=dev)
+    ms = time_calls(lambda: dsa.topk(p, sc, 0, R, idx), steps, warmup, torch.cuda.current_stream(dev))
+    assert dsa.get_status() == 0
+    _, _, byts = algorithmic(wl, np.arange(S - R, S))
+    return {"stage": "topk", "workload": wl["name"], "rows": R, "ms": ms,
+            "gbs": byts / (ms * 1e-3) / 1e9, "hbm_frac": byts / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
 
@@ -214,6 +299,9 @@ def main():
     ap.add_argument("--workload", default="dsv32_S32768", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-bwd", action="store_true", help="skip the training-shape backward timing")
+    ap.add_argument("--stage", default=None, choices=["topk"],
+                    help="time one stage alone (a profiling aid; prints its own JSON line)")
     args = ap.parse_args()
     wl = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
@@ -232,6 +320,9 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     import sparse_attention_long_gb300 as dsa
+    if args.stage == "topk":
+        print(json.dumps(topk_stage(dsa, dev, wl, args.steps, args.warmup, load_peaks())), flush=True)
+        return
 
     S, k = wl["S"], wl["topk"]
     x = synth.make_inputs(wl, device=dev, seed=rank)   # each rank: its own replica problem
@@ -346,6 +437,11 @@ def main():
                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
         assert dsa.get_status() == 0
 
+    bwd = None
+    if not args.no_bwd and rank == 0:
+        del x, out, ring, idx, m, l, flush
+        torch.cuda.empty_cache()
+        bwd = backward_stage(dsa, dev, max(2, min(K, 5)), peak_tc)
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -379,6 +475,7 @@ def main():
         "wall_s_timed": t_wall,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "backward": bwd,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
