@@ -183,9 +183,9 @@ int dsa_sparse_attn_bwd(const dsa_params *p, const void *q, const void *kv, cons
  *       accumulation of dk_I; NULL allowed when the size is 0).
  *   bf16 path: the attention shapes of dsa_sparse_attn_bwd plus H_I 64,
  *       d_I 128, else DSA_ERR_UNSUPPORTED; q, kv, k_I, dk_I and the workspace
- *       16-byte aligned, dq_I 4-byte aligned.  The workspace holds the
- *       head-summed probabilities, dI and the indexer logits S, all fp32:
- *       8 * rows * topk + 256 * rows * topk + 256 bytes.
+ *       16-byte aligned, dq_I 4-byte aligned, topk <= 2048.  The workspace
+ *       holds the head-summed attention probabilities, fp32:
+ *       4 * rows * topk + 256 bytes.
  */
 int dsa_indexer_kl_loss_bwd(const dsa_params *p, const void *q, const void *kv, const void *q_I,
                             const void *k_I, const void *w, const int32_t *idx,

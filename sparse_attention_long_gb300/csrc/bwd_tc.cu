@@ -17,7 +17,8 @@
 //   dkv     dKV_sel += (scale*dS)^T Q + P^T dO   per (token, key tile, col tile),
 //           scattered with fp32 vector reductions.
 // The same scores kernel in its logits-only form gives the head-summed
-// attention probabilities the indexer KL loss needs.
+// attention probabilities the indexer KL loss needs (kl_tc.cu takes it from
+// there).
 #include <math.h>
 
 #include "dsa_common.cuh"
@@ -583,210 +584,6 @@ __global__ void __launch_bounds__(128, 1)
   }
 }
 
-// ------------------------- indexer KL loss (SIMT) ---------------------------
-// [DSA-32K] SparseLightningIndexerGradKLLoss, per query row:
-//   p  = praw / sum(praw)       (head-summed attention probabilities,
-//                                L1-normalised over the selected keys)
-//   S_j = q_I,j . k_I[idx]      (stored: the later passes need it)
-//   I  = sum_j w_j ReLU(S_j),  pi = Softmax(I) over the selected keys
-//   loss += sum p (log p - log pi),  dI = pi - p   (stored)
-// then  dS_j = dI w_j [S_j > 0],  dw_j = sum dI ReLU(S_j),
-//       dq_I = dS K_sel (kl_dq_kernel),  dk_I[idx] += dS^T q_I (kl_dk_kernel).
-constexpr int kHI = 64, kDI = 128;
-__global__ void __launch_bounds__(256)
-    kl_main_kernel(Shape s, const __nv_bfloat16* __restrict__ q_I, const __nv_bfloat16* __restrict__ k_I,
-                   const __nv_bfloat16* __restrict__ w, const int32_t* __restrict__ idx,
-                   const float* __restrict__ praw, float* __restrict__ loss,
-                   float* __restrict__ S_ws, float* __restrict__ dI_ws, DevCtx c) {
-  extern __shared__ float sh[];
-  const int k = s.topk;
-  float* qs = sh;                       // [64][128]
-  float* ws = qs + kHI * kDI;           // [64]
-  float* pv = ws + kHI;                 // [k] target p
-  float* Iv = pv + k;                   // [k] indexer logits
-  float* red = Iv + k;                  // [32]
-  const long long row = blockIdx.x;
-  const long long b = row / s.S_q;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < kHI * kDI; i += 256) qs[i] = __bfloat162float(q_I[row * kHI * kDI + i]);
-  for (int i = tid; i < kHI; i += 256) ws[i] = __bfloat162float(w[row * kHI + i]);
-  float psum = 0.f;
-  for (int i = tid; i < k; i += 256) {
-    const int id = idx[row * k + i];
-    const float pr = (id >= 0 && id < s.S_k) ? praw[row * k + i] : 0.f;
-    pv[i] = pr;
-    psum += pr;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
-  if (lane == 0) red[warp] = psum;
-  __syncthreads();
-  float P = 0.f;
-  for (int i = 0; i < 8; ++i) P += red[i];
-  const float pinv = P > 0.f ? 1.f / P : 0.f;
-  float* Srow = S_ws + row * (long long)kHI * k;
-  float imax = -INFINITY;
-  for (int i = tid; i < k; i += 256) {
-    pv[i] *= pinv;
-    const int id = idx[row * k + i];
-    float I = -INFINITY;
-    if (id >= 0 && id < s.S_k) {
-      const uint4* kr = reinterpret_cast<const uint4*>(k_I + (b * s.S_k + id) * kDI);
-      float kf[kDI];
-#pragma unroll
-      for (int q = 0; q < kDI / 8; ++q) {
-        const uint4 u = __ldg(kr + q);
-        const __nv_bfloat162* hp = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(hp[e]);
-          kf[8 * q + 2 * e] = f.x;
-          kf[8 * q + 2 * e + 1] = f.y;
-        }
-      }
-      I = 0.f;
-#pragma unroll 1
-      for (int j = 0; j < kHI; ++j) {
-        const float* qj = qs + j * kDI;
-        float d0 = 0.f, d1 = 0.f;
-#pragma unroll
-        for (int d = 0; d < kDI; d += 2) {
-          d0 = fmaf(qj[d], kf[d], d0);
-          d1 = fmaf(qj[d + 1], kf[d + 1], d1);
-        }
-        const float S = d0 + d1;
-        Srow[(long long)j * k + i] = S;
-        I = fmaf(ws[j], fmaxf(S, 0.f), I);
-      }
-    } else {
-      for (int j = 0; j < kHI; ++j) Srow[(long long)j * k + i] = 0.f;
-    }
-    Iv[i] = I;
-    imax = fmaxf(imax, I);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) imax = fmaxf(imax, __shfl_xor_sync(0xffffffffu, imax, o));
-  __syncthreads();
-  if (lane == 0) red[warp] = imax;
-  __syncthreads();
-  float Im = red[0];
-  for (int i = 1; i < 8; ++i) Im = fmaxf(Im, red[i]);
-  float es = 0.f;
-  for (int i = tid; i < k; i += 256)
-    if (Iv[i] != -INFINITY) es += expf(Iv[i] - Im);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) es += __shfl_xor_sync(0xffffffffu, es, o);
-  __syncthreads();
-  if (lane == 0) red[warp] = es;
-  __syncthreads();
-  float E = 0.f;
-  for (int i = 0; i < 8; ++i) E += red[i];
-  const float lse = Im + logf(E);
-  float lpart = 0.f;
-  for (int i = tid; i < k; i += 256) {
-    float di = 0.f;
-    if (Iv[i] != -INFINITY) {
-      const float logpi = Iv[i] - lse;
-      if (pv[i] > 0.f) lpart += pv[i] * (logf(pv[i]) - logpi);
-      di = expf(logpi) - pv[i];
-    }
-    dI_ws[row * k + i] = di;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) lpart += __shfl_xor_sync(0xffffffffu, lpart, o);
-  __syncthreads();
-  if (lane == 0) red[warp] = lpart;
-  __syncthreads();
-  if (tid == 0 && Im != -INFINITY) {
-    float L = 0.f;
-    for (int i = 0; i < 8; ++i) L += red[i];
-    atomicAdd(loss, L);
-  }
-}
-
-// dk_I[idx_i, :] += sum_j dS_ij q_I[t, j, :],  dS_ij = dI_i w_j [S_ij > 0].
-// CTA = row, thread = key slot; vector reductions into dk_I.
-__global__ void __launch_bounds__(256)
-    kl_dk_kernel(Shape s, const __nv_bfloat16* __restrict__ q_I, const __nv_bfloat16* __restrict__ w,
-                 const int32_t* __restrict__ idx, const float* __restrict__ S_ws,
-                 const float* __restrict__ dI_ws, float* __restrict__ dk_I) {
-  __shared__ float qs[kHI * kDI];
-  __shared__ float wsh[kHI];
-  const long long row = blockIdx.x;
-  const long long b = row / s.S_q;
-  const int k = s.topk;
-  for (int i = threadIdx.x; i < kHI * kDI; i += 256) qs[i] = __bfloat162float(q_I[row * kHI * kDI + i]);
-  if (threadIdx.x < kHI) wsh[threadIdx.x] = __bfloat162float(w[row * kHI + threadIdx.x]);
-  __syncthreads();
-  const float* Srow = S_ws + row * (long long)kHI * k;
-  for (int i = threadIdx.x; i < k; i += 256) {
-    const int id = idx[row * k + i];
-    if (id < 0 || id >= s.S_k) continue;
-    const float di = dI_ws[row * k + i];
-    float* dkr = dk_I + (b * s.S_k + id) * kDI;
-#pragma unroll 1
-    for (int d0 = 0; d0 < kDI; d0 += 32) {
-      float acc[32];
-#pragma unroll
-      for (int d = 0; d < 32; ++d) acc[d] = 0.f;
-      for (int j = 0; j < kHI; ++j) {
-        if (!(Srow[(long long)j * k + i] > 0.f)) continue;
-        const float g = di * wsh[j];
-        const float* qj = qs + j * kDI + d0;
-#pragma unroll
-        for (int d = 0; d < 32; ++d) acc[d] = fmaf(g, qj[d], acc[d]);
-      }
-#pragma unroll
-      for (int d = 0; d < 32; d += 4) red_add_v4(dkr + d0 + d, acc[d], acc[d + 1], acc[d + 2], acc[d + 3]);
-    }
-  }
-}
-
-// dq_I[t, j, :] = sum_i dS_ij k_I[idx_i, :] and dw[t, j] = sum_i dI_i ReLU(S_ij).
-// CTA = row; thread = (head j = tid/4, 32 dims at 32*(tid%4)).
-__global__ void __launch_bounds__(256)
-    kl_dq_kernel(Shape s, const __nv_bfloat16* __restrict__ k_I, const __nv_bfloat16* __restrict__ w,
-                 const int32_t* __restrict__ idx, const float* __restrict__ S_ws,
-                 const float* __restrict__ dI_ws, __nv_bfloat16* __restrict__ dq_I,
-                 float* __restrict__ dw) {
-  const long long row = blockIdx.x;
-  const long long b = row / s.S_q;
-  const int k = s.topk;
-  const int j = threadIdx.x >> 2, d0 = 32 * (threadIdx.x & 3);
-  const float wj = __bfloat162float(w[row * kHI + j]);
-  const float* Sr = S_ws + (row * kHI + j) * (long long)k;
-  const float* dIr = dI_ws + row * k;
-  float acc[32];
-#pragma unroll
-  for (int d = 0; d < 32; ++d) acc[d] = 0.f;
-  float dwacc = 0.f;
-  for (int i = 0; i < k; ++i) {
-    const int id = idx[row * k + i];
-    if (id < 0 || id >= s.S_k) continue;
-    const float S = Sr[i];
-    if (!(S > 0.f)) continue;
-    const float di = dIr[i];
-    dwacc = fmaf(di, S, dwacc);
-    const float g = di * wj;
-    const uint4* kr = reinterpret_cast<const uint4*>(k_I + (b * s.S_k + id) * kDI + d0);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 u = __ldg(kr + q);
-      const __nv_bfloat162* hp = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(hp[e]);
-        acc[8 * q + 2 * e] = fmaf(g, f.x, acc[8 * q + 2 * e]);
-        acc[8 * q + 2 * e + 1] = fmaf(g, f.y, acc[8 * q + 2 * e + 1]);
-      }
-    }
-  }
-  __nv_bfloat16* o = dq_I + (row * kHI + j) * kDI + d0;
-#pragma unroll
-  for (int d = 0; d < 32; d += 2) *reinterpret_cast<__nv_bfloat162*>(o + d) = __floats2bfloat162_rn(acc[d], acc[d + 1]);
-  if ((threadIdx.x & 3) == 0) dw[row * kHI + j] = dwacc;
-}
-
 }  // namespace bwd
 
 bool make_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
@@ -798,10 +595,15 @@ size_t bwd_tc_workspace(const Shape& s) {
   const size_t rh = (size_t)s.B * s.S_q * bwd::kH;
   return 4 * rh * (size_t)s.topk * 2 + rh * 4 + 256;
 }
+// the KL pass: head-summed attention probabilities [rows][k] fp32
 size_t kl_tc_workspace(const Shape& s) {
   const size_t rows = (size_t)s.B * s.S_q;
-  return 2 * rows * (size_t)s.topk * 4 + rows * bwd::kHI * (size_t)s.topk * 4 + 256;
+  return rows * (size_t)s.topk * 4 + 256;
 }
+
+int launch_kl_tc(const Shape& s, const void* q_I, const void* k_I, const void* w,
+                 const int32_t* idx, const float* praw, float* loss, void* dq_I, float* dk_I,
+                 float* dw, DevCtx c, cudaStream_t st);
 
 template <typename K>
 static bool set_smem(K kernel, size_t bytes) {
@@ -856,8 +658,6 @@ int launch_kl_bwd_tc(const Shape& s, const void* q, const void* kv, const void* 
   const long long rows = (long long)s.B * s.S_q, rh = rows * kH;
   const int k = s.topk;
   float* praw = (float*)ws;
-  float* dI = praw + rows * k;
-  float* Sw = dI + rows * k;
   const int ntile = (k + 127) / 128;
   CUtensorMap tq;
   if (!make_tmap_2d_bf16(&tq, q, rh, kDQK, 64, kH, 128)) return DSA_ERR_CUDA;
@@ -866,18 +666,8 @@ int launch_kl_bwd_tc(const Shape& s, const void* q, const void* kv, const void* 
   scores_kernel<false><<<(unsigned)(rows * ntile), kSThreads, s1, st>>>(
       tq, tq, (const __nv_bfloat16*)kv, s, idx, mx, sm, nullptr, nullptr, nullptr, nullptr, nullptr,
       praw, ntile, c);
-  const size_t sk = sizeof(float) * (size_t)(kHI * kDI + kHI + 2 * k + 32);
-  if (!set_smem(kl_main_kernel, sk)) return DSA_ERR_CUDA;
-  kl_main_kernel<<<(unsigned)rows, 256, sk, st>>>(s, (const __nv_bfloat16*)q_I,
-                                                  (const __nv_bfloat16*)k_I,
-                                                  (const __nv_bfloat16*)w, idx, praw, loss, Sw, dI,
-                                                  c);
-  kl_dk_kernel<<<(unsigned)rows, 256, 0, st>>>(s, (const __nv_bfloat16*)q_I,
-                                               (const __nv_bfloat16*)w, idx, Sw, dI, dk_I);
-  kl_dq_kernel<<<(unsigned)rows, 256, 0, st>>>(s, (const __nv_bfloat16*)k_I,
-                                               (const __nv_bfloat16*)w, idx, Sw, dI,
-                                               (__nv_bfloat16*)dq_I, dw);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+  return launch_kl_tc(s, q_I, k_I, w, idx, praw, loss, dq_I, dk_I, dw, c, st);
 }
 
 }  // namespace dsa

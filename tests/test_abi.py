@@ -73,15 +73,15 @@ def test_host_validation_without_gpu():
 
 def test_backward_workspace_sizes():
     # bf16 tensor-core backward: P and scale*dS as bf16 hi/lo pairs
-    # [rows*128][k] plus D [rows*128] fp32; the KL pass: head-summed P and dI
-    # [rows][k] plus the indexer logits [rows][64][k], fp32
+    # [rows*128][k] plus D [rows*128] fp32; the KL pass: head-summed P
+    # [rows][k] fp32
     dsa = _lib()
     rows, k = 24, 2048
     p = dsa.make_params(B=1, S_q=rows, S_k=16384, H=128, d_qk=576, d_v=512, H_I=64, d_I=128,
                         topk=k, scale=0.5, dtype="bf16")
     rh = rows * 128
     assert dsa.workspace_size(p, dsa.DSA_CALL_ATTN_BWD) == 4 * rh * k * 2 + rh * 4 + 256
-    assert dsa.workspace_size(p, dsa.DSA_CALL_KL_BWD) == 2 * rows * k * 4 + rows * 64 * k * 4 + 256
+    assert dsa.workspace_size(p, dsa.DSA_CALL_KL_BWD) == rows * k * 4 + 256
     # a k that is not a multiple of 8 has no tensor-core backward
     odd = dsa.make_params(B=1, S_q=rows, S_k=16384, H=128, d_qk=576, d_v=512, H_I=64, d_I=128,
                           topk=2047, scale=0.5, dtype="bf16")
