@@ -89,9 +89,9 @@ def time_calls(fn, steps, warmup, stream):
 
 
 def backward_stage(dsa, dev, steps, peak_tc):
-    """The training-shape backward (S = 16384, top-2048, all rows): forward once
-    for the indices and softmax statistics, then the attention backward
-    (dq, dkv) and the indexer KL-loss backward, each timed alone."""
+    """The training-shape backward (S = 16384, top-2048, all rows): the forward,
+    the attention backward (dq, dkv), the indexer KL-loss backward, each timed
+    alone, and dsa_backward (both in one call sharing the recompute of P)."""
     wl = synth.WORKLOADS["dsv32_S16384_train"]
     S, k, H = wl["S"], wl["topk"], wl["H"]
     x = synth.make_inputs(wl, device=dev, with_dout=True)
@@ -110,22 +110,29 @@ def backward_stage(dsa, dev, steps, peak_tc):
     dk_I = torch.zeros(1, S, wl["d_I"], device=dev)
     dw = torch.empty(1, S, wl["H_I"], device=dev)
     ws_k = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_KL_BWD), dtype=torch.uint8, device=dev)
+    ws_all = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_BACKWARD), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     fwd = lambda: dsa.forward(p, x["q_I"], x["k_I"], x["w"], x["q"], x["kv"], idx, out, m, l, ring)
     bwd = lambda: dsa.sparse_attn_bwd(p, x["q"], x["kv"], idx, out, x["dO"], m, l, dq, dkv, ws_b)
     kl = lambda: dsa.indexer_kl_loss_bwd(p, x["q"], x["kv"], x["q_I"], x["k_I"], x["w"], idx, m, l,
                                          loss, dq_I, dk_I, dw, ws_k)
+    both = lambda: dsa.backward(p, x["q"], x["kv"], idx, out, x["dO"], m, l, x["q_I"], x["k_I"],
+                                x["w"], dq, dkv, loss, dq_I, dk_I, dw, ws_all)
     t_fwd = time_calls(fwd, steps, 1, stream)
     t_bwd = time_calls(bwd, steps, 1, stream)
     t_kl = time_calls(kl, steps, 1, stream)
+    t_both = time_calls(both, steps, 1, stream)
     assert dsa.get_status() == 0, "device status after the backward"
     f_bwd, f_kl = algorithmic_bwd(wl, np.arange(S))
     return {"workload": wl["name"], "calls_timed": steps,
             "forward_ms": t_fwd, "attn_bwd_ms": t_bwd, "kl_bwd_ms": t_kl,
+            "backward_ms": t_both,
+            "backward_tflops": (f_bwd + f_kl) / (t_both * 1e-3) / 1e12,
             "attn_bwd_tflops": f_bwd / (t_bwd * 1e-3) / 1e12,
             "kl_bwd_tflops": f_kl / (t_kl * 1e-3) / 1e12,
             "attn_bwd_frac": f_bwd / (t_bwd * 1e-3) / 1e12 / peak_tc,
-            "workspace_bytes": {"attn_bwd": ws_b.numel(), "kl_bwd": ws_k.numel()},
+            "workspace_bytes": {"attn_bwd": ws_b.numel(), "kl_bwd": ws_k.numel(),
+                                "backward": ws_all.numel()},
             "note": "outside the timed forward step; dkv / dk_I accumulate over calls"}
 
 
@@ -300,7 +307,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-bwd", action="store_true", help="skip the training-shape backward timing")
-    ap.add_argument("--stage", default=None, choices=["topk"],
+    ap.add_argument("--stage", default=None, choices=["topk", "bwd"],
                     help="time one stage alone (a profiling aid; prints its own JSON line)")
     args = ap.parse_args()
     wl = synth.WORKLOADS[args.workload]
@@ -322,6 +329,10 @@ def main():
     import sparse_attention_long_gb300 as dsa
     if args.stage == "topk":
         print(json.dumps(topk_stage(dsa, dev, wl, args.steps, args.warmup, load_peaks())), flush=True)
+        return
+    if args.stage == "bwd":
+        bwd = backward_stage(dsa, dev, args.steps, load_peaks()["bf16_tflops_sustained"])
+        print(json.dumps(dict(stage="bwd", **bwd)), flush=True)
         return
 
     S, k = wl["S"], wl["topk"]

@@ -74,7 +74,13 @@ enum { DSA_CP_COLOSSAL = 0, DSA_CP_ULYSSES = 1 };
 enum { DSA_FLAG_CAUSAL_ONLY = 1 };
 
 /* workspace queries (dsa_workspace_size `which`) */
-enum { DSA_CALL_FORWARD = 0, DSA_CALL_ATTN_FWD = 1, DSA_CALL_ATTN_BWD = 2, DSA_CALL_KL_BWD = 3 };
+enum {
+  DSA_CALL_FORWARD = 0,
+  DSA_CALL_ATTN_FWD = 1,
+  DSA_CALL_ATTN_BWD = 2,
+  DSA_CALL_KL_BWD = 3,
+  DSA_CALL_BACKWARD = 4
+};
 
 typedef struct {
   int32_t layout;              /* DSA_BSND or DSA_TND (TND requires B == 1)            */
@@ -192,6 +198,26 @@ int dsa_indexer_kl_loss_bwd(const dsa_params *p, const void *q, const void *kv, 
                             const float *softmax_max, const float *softmax_sum, float *loss,
                             void *dq_I, float *dk_I, float *dw, void *workspace,
                             dsa_stream_t stream);
+
+/*
+ * Whole backward of one training step: dsa_sparse_attn_bwd and
+ * dsa_indexer_kl_loss_bwd in one call, with the results of calling the two
+ * one after the other.  [DSA-32K] SparseFlashAttentionGrad recomputes the
+ * attention probabilities P and SparseLightningIndexerGradKLLoss needs their
+ * head sum as its target; here the attention pass writes that sum while it has
+ * P at hand, so the KL pass does not recompute the attention logits.
+ *   Arguments, layouts, accumulation (dkv, loss, dk_I are ACCUMULATED; dq,
+ *   dq_I, dw written) and alignment as in the two calls above.
+ *   workspace: dsa_workspace_size(p, DSA_CALL_BACKWARD) bytes (bf16 path:
+ *       the attention backward's workspace followed by the [rows][topk] fp32
+ *       target; fp32 path: the larger of the two calls' workspaces, used by
+ *       each in turn).
+ */
+int dsa_backward(const dsa_params *p, const void *q, const void *kv, const int32_t *idx,
+                 const void *out, const void *dout, const float *softmax_max,
+                 const float *softmax_sum, const void *q_I, const void *k_I, const void *w,
+                 void *dq, float *dkv, float *loss, void *dq_I, float *dk_I, float *dw,
+                 void *workspace, dsa_stream_t stream);
 
 /*
  * Whole forward: indexer scores -> top-k -> sparse attention, the S x S score

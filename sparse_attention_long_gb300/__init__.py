@@ -20,7 +20,7 @@ DSA_ERR_CUDA, DSA_ERR_TIMEOUT, DSA_ERR_INDEX = -4, -5, -6
 DSA_BSND, DSA_TND = 0, 1
 DSA_BF16, DSA_FP32 = 0, 1
 DSA_CP_COLOSSAL, DSA_CP_ULYSSES = 0, 1
-DSA_CALL_FORWARD, DSA_CALL_ATTN_FWD, DSA_CALL_ATTN_BWD, DSA_CALL_KL_BWD = 0, 1, 2, 3
+DSA_CALL_FORWARD, DSA_CALL_ATTN_FWD, DSA_CALL_ATTN_BWD, DSA_CALL_KL_BWD, DSA_CALL_BACKWARD = 0, 1, 2, 3, 4
 DSA_FLAG_CAUSAL_ONLY = 1
 
 _ERRNAMES = {0: "DSA_OK", -1: "DSA_ERR_INVALID_ARG", -2: "DSA_ERR_UNSUPPORTED",
@@ -59,6 +59,7 @@ _sigs = {
     "dsa_sparse_attn_fwd": ([_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
     "dsa_sparse_attn_bwd": ([_P] + [_vp] * 11, ctypes.c_int),
     "dsa_indexer_kl_loss_bwd": ([_P] + [_vp] * 14, ctypes.c_int),
+    "dsa_backward": ([_P] + [_vp] * 18, ctypes.c_int),
     "dsa_forward": ([_P] + [_vp] * 11, ctypes.c_int),
     "dsa_forward_static_ws": ([_P] + [_vp] * 10, ctypes.c_int),
     "dsa_get_status": ([_vp, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
@@ -156,6 +157,15 @@ def indexer_kl_loss_bwd(p, q, kv, q_I, k_I, w, idx, softmax_max, softmax_sum, lo
                                      _ptr(w), _ptr(idx), _ptr(softmax_max), _ptr(softmax_sum),
                                      _ptr(loss), _ptr(dq_I), _ptr(dk_I), _ptr(dw),
                                      _ptr(workspace), _stream(stream)), "dsa_indexer_kl_loss_bwd")
+
+
+def backward(p, q, kv, idx, out, dout, softmax_max, softmax_sum, q_I, k_I, w, dq, dkv, loss, dq_I,
+             dk_I, dw, workspace=None, stream=None):
+    """sparse_attn_bwd and indexer_kl_loss_bwd in one call sharing the recompute of P."""
+    _chk(lib.dsa_backward(ctypes.byref(p), _ptr(q), _ptr(kv), _ptr(idx), _ptr(out), _ptr(dout),
+                          _ptr(softmax_max), _ptr(softmax_sum), _ptr(q_I), _ptr(k_I), _ptr(w),
+                          _ptr(dq), _ptr(dkv), _ptr(loss), _ptr(dq_I), _ptr(dk_I), _ptr(dw),
+                          _ptr(workspace), _stream(stream)), "dsa_backward")
 
 
 def forward(p, q_I, k_I, w, q, kv, idx_out, out, softmax_max, softmax_sum, workspace, stream=None):

@@ -34,9 +34,15 @@ int launch_attn_fwd_tc(const Shape& s, const void* q, const void* kv, const int3
                        float* mx, float* sm, DevCtx c, cudaStream_t st);
 size_t bwd_tc_workspace(const Shape& s);
 size_t kl_tc_workspace(const Shape& s);
+int launch_dsa_bwd_tc(const Shape& s, const void* q, const void* kv, const int32_t* idx,
+                      const void* out, const void* dout, const float* mx, const float* sm,
+                      const void* q_I, const void* k_I, const void* w, void* dq, float* dkv,
+                      float* loss, void* dq_I, float* dk_I, float* dw, void* ws, DevCtx c,
+                      cudaStream_t st);
 int launch_attn_bwd_tc(const Shape& s, const void* q, const void* kv, const int32_t* idx,
                        const void* out, const void* dout, const float* mx, const float* sm,
-                       void* dq, float* dkv, void* ws, DevCtx c, cudaStream_t st);
+                       void* dq, float* dkv, void* ws, DevCtx c, cudaStream_t st,
+                       float* praw);
 int launch_kl_bwd_tc(const Shape& s, const void* q, const void* kv, const void* q_I,
                      const void* k_I, const void* w, const int32_t* idx, const float* mx,
                      const float* sm, float* loss, void* dq_I, float* dk_I, float* dw, void* ws,
@@ -196,6 +202,11 @@ size_t dsa_workspace_size(const dsa_params* p, int which) {
   if (which == DSA_CALL_FORWARD) return (size_t)wave_rows(p) * (size_t)p->S_k * sizeof(float);
   if (which == DSA_CALL_ATTN_BWD && tc_bwd_shape(p)) return bwd_tc_workspace(s);
   if (which == DSA_CALL_KL_BWD && tc_bwd_shape(p) && tc_indexer_shape(p)) return kl_tc_workspace(s);
+  if (which == DSA_CALL_BACKWARD) {
+    if (tc_bwd_shape(p) && tc_indexer_shape(p)) return bwd_tc_workspace(s) + kl_tc_workspace(s);
+    const size_t a = dsa_workspace_size(p, DSA_CALL_ATTN_BWD), b = dsa_workspace_size(p, DSA_CALL_KL_BWD);
+    return a > b ? a : b;  // the exact path runs the two passes one after the other
+  }
   // the exact (fp32) path accumulates dkv / dk_I in fp64 before adding them
   if (which == DSA_CALL_ATTN_BWD && p->dtype == DSA_FP32)
     return (size_t)(p->B * p->S_k * p->d_qk) * sizeof(double);
@@ -263,7 +274,7 @@ int dsa_sparse_attn_bwd(const dsa_params* p, const void* q, const void* kv, cons
     DevCtx c;
     if (!dev_ctx(&c)) return DSA_ERR_CUDA;
     return launch_attn_bwd_tc(s, q, kv, idx, out, dout, softmax_max, softmax_sum, dq, dkv,
-                              workspace, c, (cudaStream_t)stream);
+                              workspace, c, (cudaStream_t)stream, nullptr);
   }
   if (p->dtype == DSA_BF16 || simt_smem_attn_bwd(s) > 200 * 1024) return DSA_ERR_UNSUPPORTED;
   if (dsa_workspace_size(p, DSA_CALL_ATTN_BWD) > 0 && !aligned16(workspace)) return DSA_ERR_WORKSPACE;
@@ -301,6 +312,34 @@ int dsa_indexer_kl_loss_bwd(const dsa_params* p, const void* q, const void* kv, 
   return launch_simt_kl_bwd(s, p->dtype == DSA_BF16, q, kv, q_I, k_I, w, idx, softmax_max,
                             softmax_sum, loss, dq_I, dk_I, dw, (double*)workspace, c,
                             (cudaStream_t)stream);
+}
+
+int dsa_backward(const dsa_params* p, const void* q, const void* kv, const int32_t* idx,
+                 const void* out, const void* dout, const float* softmax_max,
+                 const float* softmax_sum, const void* q_I, const void* k_I, const void* w,
+                 void* dq, float* dkv, float* loss, void* dq_I, float* dk_I, float* dw,
+                 void* workspace, dsa_stream_t stream) {
+  Shape s;
+  int rc = check_params(p, &s);
+  if (rc) return rc;
+  if (!q || !kv || !idx || !out || !dout || !softmax_max || !softmax_sum || !q_I || !k_I || !w ||
+      !dq || !dkv || !loss || !dq_I || !dk_I || !dw)
+    return DSA_ERR_INVALID_ARG;
+  if (tc_bwd_shape(p) && tc_indexer_shape(p)) {
+    if (!aligned16(q) || !aligned16(kv) || !aligned16(out) || !aligned16(dout) || !aligned16(dq) ||
+        !aligned16(dkv) || !aligned16(k_I) || !aligned16(dk_I) || ((uintptr_t)dq_I & 3u) != 0)
+      return DSA_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace)) return DSA_ERR_WORKSPACE;
+    DevCtx c;
+    if (!dev_ctx(&c)) return DSA_ERR_CUDA;
+    return launch_dsa_bwd_tc(s, q, kv, idx, out, dout, softmax_max, softmax_sum, q_I, k_I, w, dq,
+                             dkv, loss, dq_I, dk_I, dw, workspace, c, (cudaStream_t)stream);
+  }
+  rc = dsa_sparse_attn_bwd(p, q, kv, idx, out, dout, softmax_max, softmax_sum, dq, dkv, workspace,
+                           stream);
+  if (rc) return rc;
+  return dsa_indexer_kl_loss_bwd(p, q, kv, q_I, k_I, w, idx, softmax_max, softmax_sum, loss, dq_I,
+                                 dk_I, dw, workspace, stream);
 }
 
 int dsa_forward(const dsa_params* p, const void* q_I, const void* k_I, const void* w,

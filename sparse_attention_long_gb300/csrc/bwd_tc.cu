@@ -266,14 +266,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
             o_dl[i] = dl[i];
           }
         }
-      } else {
+      }
+      if (!kGrad || praw) {
         // transpose through shared memory, [key][head] with a 129-float row
-        // pitch (conflict-free writes by head and reads by key)
+        // pitch (conflict-free writes by head and reads by key); the kv tile
+        // is no longer needed once the MMAs are done
 #pragma unroll
         for (int i = 0; i < 32; ++i) T[(cc + i) * (kH + 1) + h] = p[i];
       }
     }
-    if (!kGrad) {
+    if (!kGrad || praw) {
       named_bar_sync(1, 128);
       const int key = h;  // thread = key: sum its row over the 128 heads
       float acc = 0.f;
@@ -611,9 +613,12 @@ static bool set_smem(K kernel, size_t bytes) {
          cudaSuccess;
 }
 
+// praw (optional, [rows][k] fp32): also write the head-summed probabilities
+// the indexer KL loss takes as its target
 int launch_attn_bwd_tc(const Shape& s, const void* q, const void* kv, const int32_t* idx,
                        const void* out, const void* dout, const float* mx, const float* sm,
-                       void* dq, float* dkv, void* ws, DevCtx c, cudaStream_t st) {
+                       void* dq, float* dkv, void* ws, DevCtx c, cudaStream_t st,
+                       float* praw) {
   using namespace bwd;
   const long long rows = (long long)s.B * s.S_q, rh = rows * kH;
   const int k = s.topk;
@@ -641,7 +646,7 @@ int launch_attn_bwd_tc(const Shape& s, const void* q, const void* kv, const int3
   if (!set_smem(scores_kernel<true>, s1) || !set_smem(dq_kernel, s2) || !set_smem(dkv_kernel, s3))
     return DSA_ERR_CUDA;
   scores_kernel<true><<<(unsigned)(rows * ntile), kSThreads, s1, st>>>(
-      tq, tdo, (const __nv_bfloat16*)kv, s, idx, mx, sm, D, P_ws, Plo_ws, dS_ws, dSlo_ws, nullptr,
+      tq, tdo, (const __nv_bfloat16*)kv, s, idx, mx, sm, D, P_ws, Plo_ws, dS_ws, dSlo_ws, praw,
       ntile, c);
   dq_kernel<<<(unsigned)(rows * 3), 192, s2, st>>>(tds, tdslo, (const __nv_bfloat16*)kv, s, idx,
                                                     (__nv_bfloat16*)dq, c);
@@ -667,6 +672,19 @@ int launch_kl_bwd_tc(const Shape& s, const void* q, const void* kv, const void* 
       tq, tq, (const __nv_bfloat16*)kv, s, idx, mx, sm, nullptr, nullptr, nullptr, nullptr, nullptr,
       praw, ntile, c);
   if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+  return launch_kl_tc(s, q_I, k_I, w, idx, praw, loss, dq_I, dk_I, dw, c, st);
+}
+
+// Attention backward and indexer KL backward sharing one recompute of P: the
+// attention pass writes the head-summed probabilities, the KL pass reads them.
+int launch_dsa_bwd_tc(const Shape& s, const void* q, const void* kv, const int32_t* idx,
+                      const void* out, const void* dout, const float* mx, const float* sm,
+                      const void* q_I, const void* k_I, const void* w, void* dq, float* dkv,
+                      float* loss, void* dq_I, float* dk_I, float* dw, void* ws, DevCtx c,
+                      cudaStream_t st) {
+  float* praw = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + bwd_tc_workspace(s));
+  const int rc = launch_attn_bwd_tc(s, q, kv, idx, out, dout, mx, sm, dq, dkv, ws, c, st, praw);
+  if (rc) return rc;
   return launch_kl_tc(s, q_I, k_I, w, idx, praw, loss, dq_I, dk_I, dw, c, st);
 }
 

@@ -44,7 +44,7 @@ struct __align__(1024) Smem {
   float iv[kMaxK];              // indexer logit I, then dI
   int32_t idx[kMaxK];
   float wv[kHI];
-  float dws[kHI];
+  float dws[4][kHI];            // per-warp dw partials (summed in a fixed order)
   float red[8];
   uint64_t kt_full, s_done, ds_full, g_done;
   uint32_t tmem_base;
@@ -122,7 +122,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   if (threadIdx.x < kHI) {
     sm.wv[threadIdx.x] = __bfloat162float(w[row * kHI + threadIdx.x]);
-    sm.dws[threadIdx.x] = 0.f;
   }
   if (last >= 0) atomicMax(&sm.last, last);
   __syncthreads();
@@ -341,10 +340,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         float v = dwp[j];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) atomicAdd(&sm.dws[j], v);
+        if (lane == 0) sm.dws[warp - 1][j] = v;
       }
       named_bar_sync(1, 128);
-      if (t < kHI) dw[row * kHI + t] = sm.dws[t];
+      if (t < kHI) dw[row * kHI + t] = ((sm.dws[0][t] + sm.dws[1][t]) + sm.dws[2][t]) + sm.dws[3][t];
     }
   }
   tc_fence_before();

@@ -82,6 +82,9 @@ def test_backward_workspace_sizes():
     rh = rows * 128
     assert dsa.workspace_size(p, dsa.DSA_CALL_ATTN_BWD) == 4 * rh * k * 2 + rh * 4 + 256
     assert dsa.workspace_size(p, dsa.DSA_CALL_KL_BWD) == rows * k * 4 + 256
+    # the fused backward: the attention backward's workspace, then the KL target
+    assert dsa.workspace_size(p, dsa.DSA_CALL_BACKWARD) == \
+        (4 * rh * k * 2 + rh * 4 + 256) + (rows * k * 4 + 256)
     # a k that is not a multiple of 8 has no tensor-core backward
     odd = dsa.make_params(B=1, S_q=rows, S_k=16384, H=128, d_qk=576, d_v=512, H_I=64, d_I=128,
                           topk=2047, scale=0.5, dtype="bf16")

@@ -49,6 +49,12 @@ def _run_case(wl, rows):
     ws2 = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_KL_BWD), dtype=torch.uint8, device=DEV)
     dsa.indexer_kl_loss_bwd(p, g["q"], g["kv"], g["q_I"], g["k_I"], g["w"], gidx, m32.to(DEV),
                             l32.to(DEV), loss, dqI, dkI, dw, ws2)
+    # the same through dsa_backward (one call, shared recompute of P)
+    f = dict(dq=torch.empty_like(dq), dkv=torch.zeros_like(dkv), loss=torch.zeros(1, device=DEV),
+             dqI=torch.empty_like(dqI), dkI=torch.zeros_like(dkI), dw=torch.empty_like(dw))
+    ws3 = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_BACKWARD), dtype=torch.uint8, device=DEV)
+    dsa.backward(p, g["q"], g["kv"], gidx, O16.to(DEV), g["dO"], m32.to(DEV), l32.to(DEV), g["q_I"],
+                 g["k_I"], g["w"], f["dq"], f["dkv"], f["loss"], f["dqI"], f["dkI"], f["dw"], ws3)
     torch.cuda.synchronize()
     assert dsa.get_status() == 0
 
@@ -57,11 +63,21 @@ def _run_case(wl, rows):
                                          l32.double().numpy(), wl["scale"], wl["d_v"])
     kl_r = oracle.indexer_kl_loss(x["q"], x["kv"], idx, m32.double().numpy(),
                                   l32.double().numpy(), wl["scale"], x["q_I"], x["k_I"], x["w"])
-    return dict(dq=(np64(dq), dq_r), dkv=(np64(dkv), dkv_r), loss=(float(loss), kl_r[0]),
-                dqI=(np64(dqI), kl_r[1]), dkI=(np64(dkI), kl_r[2]), dw=(np64(dw), kl_r[3]))
+    sep = dict(dq=(np64(dq), dq_r), dkv=(np64(dkv), dkv_r), loss=(float(loss), kl_r[0]),
+               dqI=(np64(dqI), kl_r[1]), dkI=(np64(dkI), kl_r[2]), dw=(np64(dw), kl_r[3]))
+    fused = dict(dq=(np64(f["dq"]), dq_r), dkv=(np64(f["dkv"]), dkv_r), loss=(float(f["loss"]), kl_r[0]),
+                 dqI=(np64(f["dqI"]), kl_r[1]), dkI=(np64(f["dkI"]), kl_r[2]), dw=(np64(f["dw"]), kl_r[3]))
+    # outputs written without atomics must match the separate calls bit for bit
+    assert torch.equal(f["dq"], dq) and torch.equal(f["dqI"], dqI) and torch.equal(f["dw"], dw)
+    return sep, fused
 
 
-def _check(res):
+def _check(both):
+    for res in both:
+        _check_one(res)
+
+
+def _check_one(res):
     for key in ("dq", "dkv", "dqI", "dkI", "dw"):
         got, ref = res[key]
         ok, ma, mr = bf16_close(got, ref)
