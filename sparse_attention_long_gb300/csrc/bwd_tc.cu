@@ -71,25 +71,29 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
 }
 
 // ------------------------------- scores ------------------------------------
-// CTA = (row, 128-key tile).  warp 0: TMEM + MMA; warp 1: TMA of q / dO column
-// chunks (64 columns x 128 heads, 3-stage ring); warps 2..5: gather the tile's
-// 128 kv rows (all 576 columns, K-major SW128, 9 chunks), then the epilogue
-// (thread = head).
+// CTA = (row, 128-key tile).  The contraction runs over 9 column chunks of 64
+// (8 latent + rope) through a 2-stage ring; stage i holds the tile's kv chunk
+// i (gathered), q chunk i and, for the gradient, dO chunk i (TMA), so chunk i
+// of kv serves both S and dP before its stage is released.  ~97 KB of shared
+// memory and 256 TMEM columns let two CTAs share an SM.  warp 0: TMEM + MMA;
+// warp 1: TMA of the q / dO chunks; warps 2..5: gather the kv chunks, then the
+// epilogue (thread = head).
 constexpr int kSTile = 128;
 constexpr int kSThreads = 192;
-constexpr int kSStages = 3;
+constexpr int kSStages = 2;
+constexpr int kSChunk = kSTile * 128;            // 16 KB: 128 rows x 64 columns
 struct __align__(1024) ScoresSmem {
-  uint8_t kv[9][kSTile * 128];     // 144 KB; reused as a [128 keys][129] fp32 transpose buffer
-  uint8_t a[kSStages][kH * 128];   // 48 KB
+  uint8_t st[kSStages][3][kSChunk];  // [stage][kv | q | dO]; reused as a [128 keys][129] fp32 buffer
   int32_t idx[kSTile];
   uint32_t mask[kSTile / 32];
-  uint64_t a_full[kSStages], a_empty[kSStages], kv_full, done;
+  uint64_t full[kSStages], empty[kSStages], done;
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(ScoresSmem) >= kSTile * (kH + 1) * 4, "transpose buffer");
 
 template <bool kGrad>
-__global__ void __launch_bounds__(kSThreads, 1)
+__global__ void __launch_bounds__(kSThreads, 2)
     scores_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __nv_bfloat16* __restrict__ kv, Shape s, const int32_t* __restrict__ idx,
                   const float* __restrict__ mx, const float* __restrict__ lsum,
@@ -107,14 +111,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int k = s.topk;
   const int slot0 = tile * kSTile;
   volatile int* abort_flag = &sm.abort;
-  constexpr int nA = kGrad ? 17 : 9;  // 9 q chunks (+ 8 dO chunks)
+  constexpr int nC = 9;  // column chunks: 8 latent (S and dP) + 1 rope (S only)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSStages; ++i) {
-      mbar_init(smem_u32(&sm.a_full[i]), 1);
-      mbar_init(smem_u32(&sm.a_empty[i]), 1);
+      mbar_init(smem_u32(&sm.full[i]), 1 + 128);  // TMA arrive (+ bytes) and the gatherers
+      mbar_init(smem_u32(&sm.empty[i]), 1);
     }
-    mbar_init(smem_u32(&sm.kv_full), 128);
     mbar_init(smem_u32(&sm.done), 1);
     sm.abort = 0;
     fence_mbar_init();
@@ -144,70 +147,67 @@ __global__ void __launch_bounds__(kSThreads, 1)
         tma_prefetch_desc(&tm_q);
         if (kGrad) tma_prefetch_desc(&tm_do);
         const int y = (int)(row * kH);
-        for (int i = 0; i < nA; ++i) {
+        for (int i = 0; i < nC; ++i) {
           const int st = i % kSStages;
-          if (!mbar_wait(smem_u32(&sm.a_empty[st]), ((i / kSStages) & 1) ^ 1, c, abort_flag)) break;
-          const uint32_t fb = smem_u32(&sm.a_full[st]);
-          mbar_arrive_expect_tx(fb, kH * 128);
-          if (i < 9) tma_load_2d(smem_u32(sm.a[st]), &tm_q, 64 * i, y, fb);
-          else tma_load_2d(smem_u32(sm.a[st]), &tm_do, 64 * (i - 9), y, fb);
+          if (!mbar_wait(smem_u32(&sm.empty[st]), ((i / kSStages) & 1) ^ 1, c, abort_flag)) break;
+          const uint32_t fb = smem_u32(&sm.full[st]);
+          const bool with_do = kGrad && i < 8;
+          mbar_arrive_expect_tx(fb, (with_do ? 2 : 1) * kSChunk);
+          tma_load_2d(smem_u32(sm.st[st][1]), &tm_q, 64 * i, y, fb);
+          if (with_do) tma_load_2d(smem_u32(sm.st[st][2]), &tm_do, 64 * i, y, fb);
         }
-        for (int i = (nA > kSStages ? nA - kSStages : 0); i < nA; ++i)  // drain
-          mbar_wait(smem_u32(&sm.a_full[i % kSStages]), (i / kSStages) & 1, c, abort_flag);
+        for (int i = nC - kSStages; i < nC; ++i)  // drain: no copy left in flight
+          mbar_wait(smem_u32(&sm.full[i % kSStages]), (i / kSStages) & 1, c, abort_flag);
       }
     } else if (warp >= 2) {
-      // gather: warp gw owns keys gw, gw+4, ...; lane = 16-byte chunk (72 per row)
-      const int gw = warp - 2;
+      // gather chunk i of the tile's 128 kv rows: thread = (key, 16-byte piece)
+      const int t = threadIdx.x - 64;
+      const int cc = t & 7;
       const __nv_bfloat16* kvb = kv + b * s.S_k * (long long)kDQK;
-      const uint32_t kvs = smem_u32(sm.kv);
-#pragma unroll 1
-      for (int m0 = 0; m0 < 32; m0 += 8) {
-        uint4 r[8][3];
+      for (int i = 0; i < nC; ++i) {
+        const int st = i % kSStages;
+        if (!mbar_wait_warp(smem_u32(&sm.empty[st]), ((i / kSStages) & 1) ^ 1, c, abort_flag)) break;
+        uint4 r[8];
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
-          const int key = gw + 4 * (m0 + m);
+          const int key = (t >> 3) + 16 * m;
           const int id = sm.idx[key] < 0 ? 0 : sm.idx[key];
-          const uint4* src = reinterpret_cast<const uint4*>(kvb + (long long)id * kDQK);
-#pragma unroll
-          for (int q = 0; q < 3; ++q)
-            if (lane + 32 * q < 72) r[m][q] = __ldg(src + lane + 32 * q);
+          r[m] = __ldg(reinterpret_cast<const uint4*>(kvb + (long long)id * kDQK + 64 * i) + cc);
         }
+        const uint32_t kvs = smem_u32(sm.st[st][0]);
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
-          const int key = gw + 4 * (m0 + m);
-#pragma unroll
-          for (int q = 0; q < 3; ++q) {
-            const int ch = lane + 32 * q;
-            if (ch < 72) {
-              const int g = ch >> 3, cc = ch & 7;
-              const uint32_t dst = kvs + g * (kSTile * 128) + key * 128 + ((cc ^ (key & 7)) << 4);
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(r[m][q].x),
-                           "r"(r[m][q].y), "r"(r[m][q].z), "r"(r[m][q].w)
-                           : "memory");
-            }
-          }
+          const int key = (t >> 3) + 16 * m;
+          const uint32_t dst = kvs + key * 128 + ((cc ^ (key & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(r[m].x),
+                       "r"(r[m].y), "r"(r[m].z), "r"(r[m].w)
+                       : "memory");
         }
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&sm.full[st]));
       }
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&sm.kv_full));
     } else if (lane == 0) {
       // MMA: S (TMEM cols 0..127) and dP (cols 128..255), M=128 heads, N=128 keys
       constexpr uint32_t idesc = idesc_bf16(128, kSTile, false, false);
-      bool ok = mbar_wait(smem_u32(&sm.kv_full), 0, c, abort_flag);
-      const uint32_t kvs = smem_u32(sm.kv);
-      for (int i = 0; ok && i < nA; ++i) {
+      bool ok = true;
+      for (int i = 0; ok && i < nC; ++i) {
         const int st = i % kSStages;
-        if (!mbar_wait(smem_u32(&sm.a_full[st]), (i / kSStages) & 1, c, abort_flag)) break;
+        ok = mbar_wait(smem_u32(&sm.full[st]), (i / kSStages) & 1, c, abort_flag);
+        if (!ok) break;
         tc_fence_after();
-        const uint32_t d = tmem + (i < 9 ? 0u : 128u);
-        const int kc = i < 9 ? i : i - 9;
-        const uint32_t a0 = smem_u32(sm.a[st]);
+        const uint32_t kv0 = smem_u32(sm.st[st][0]), q0 = smem_u32(sm.st[st][1]),
+                       o0 = smem_u32(sm.st[st][2]);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ss(d, sdesc(a0 + kk * 32, 16, 1024, kSw128),
-                      sdesc(kvs + kc * (kSTile * 128) + kk * 32, 16, 1024, kSw128), idesc,
-                      (i != 0 && i != 9) || kk > 0 ? 1u : 0u);
-        mma_commit(smem_u32(&sm.a_empty[st]));
+          mma_bf16_ss(tmem, sdesc(q0 + kk * 32, 16, 1024, kSw128),
+                      sdesc(kv0 + kk * 32, 16, 1024, kSw128), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        if (kGrad && i < 8) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(tmem + 128, sdesc(o0 + kk * 32, 16, 1024, kSw128),
+                        sdesc(kv0 + kk * 32, 16, 1024, kSw128), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&sm.empty[st]));
       }
       mma_commit(smem_u32(&sm.done));
     }
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const float linv = lv > 0.f ? 1.f / lv : 0.f;
     const float sl2e = s.scale * kLog2e;
     const float Dh = kGrad ? Dg[rh] : 0.f;
-    float* T = reinterpret_cast<float*>(sm.kv);  // colsum mode: [128 heads][128 keys]
+    float* T = reinterpret_cast<float*>(sm.st);  // colsum mode: [128 keys][129]
 #pragma unroll 1
     for (int cc = 0; cc < kSTile; cc += 32) {
       uint32_t sv[32], dv[32];
@@ -450,16 +450,18 @@ __global__ void __launch_bounds__(192, 1)
 // --------------------------------- dkv --------------------------------------
 // CTA = (row, 128-key tile, column tile n: [0,256) | [256,512) | [512,576)).
 // D[128 keys x N] = (scale*dS)^T Q (+ P^T dO for value columns), contracted
-// over the 128 heads in four chunks of 32 through a 3-stage TMA ring.  P and
+// over the 128 heads in eight chunks of 16 through a 3-stage TMA ring (96 KB of
+// shared memory, so two CTAs share an SM and one's reductions overlap the
+// other's loads and MMAs).  P and
 // scale*dS enter as bf16 pairs hi + lo (a single bf16 rounding of P or dS
 // would leave the accumulated dKV of early keys about 0.1 off at this size).
 // Both operands are MN-major straight from TMA boxes (64 keys or 64 columns
-// by 32 heads).  warp 1 lane 0: TMA; warp 0 lane 0: MMA; then all four warps
+// by 16 heads).  warp 1 lane 0: TMA; warp 0 lane 0: MMA; then all four warps
 // drain TMEM (thread = key) and scatter-add their rows into dkv with vector
 // reductions.
 constexpr int kVStages = 3;
-constexpr int kVHeads = 32;                 // heads per stage
-constexpr int kVBox = 64 * kVHeads * 2;     // 4 KB: 64 keys (or columns) x 32 heads
+constexpr int kVHeads = 16;                 // heads per stage
+constexpr int kVBox = 64 * kVHeads * 2;     // 2 KB: 64 keys (or columns) x 16 heads
 struct __align__(1024) DkvSmem {
   uint8_t a[kVStages][4][2][kVBox];         // [dS hi, dS lo, P hi, P lo][key half]
   uint8_t bq[kVStages][4][kVBox];           // q columns, 4 boxes of 64
@@ -471,7 +473,7 @@ struct __align__(1024) DkvSmem {
   int abort;
 };
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(128, 2)
     dkv_kernel(const __grid_constant__ CUtensorMap tm_ds, const __grid_constant__ CUtensorMap tm_dslo,
                const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_plo,
                const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
