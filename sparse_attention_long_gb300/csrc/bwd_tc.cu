@@ -224,7 +224,15 @@ __global__ void __launch_bounds__(kSThreads, 2)
     const float linv = lv > 0.f ? 1.f / lv : 0.f;
     const float sl2e = s.scale * kLog2e;
     const float Dh = kGrad ? Dg[rh] : 0.f;
-    float* T = reinterpret_cast<float*>(sm.st);  // colsum mode: [128 keys][129]
+    // The ring is free once the MMAs are done: it stages each 32-key chunk of
+    // the four bf16 outputs ([array][head][32 keys], 80-byte row pitch) so the
+    // global stores go out as whole 64-byte row segments, and keeps the
+    // per-warp head sums of P ([quadrant][key]) for the KL target.
+    constexpr int kPitch = 80;
+    uint8_t* stg = &sm.st[0][0][0];
+    float* psum = reinterpret_cast<float*>(stg + 4 * kH * kPitch);
+    const bool colsum = !kGrad || praw != nullptr;
+    const int t = threadIdx.x - 64;
 #pragma unroll 1
     for (int cc = 0; cc < kSTile; cc += 32) {
       uint32_t sv[32], dv[32];
@@ -243,43 +251,57 @@ __global__ void __launch_bounds__(kSThreads, 2)
         // P and scale*dS as bf16 pairs hi + lo, hi = bf16(x), lo = bf16(x - hi):
         // the later passes contract both halves, so the products carry ~16
         // mantissa bits of P and dS instead of 8
-        uint4 ph[4], pl[4], dh[4], dl[4];
+        uint32_t pk[4][16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float d0 = have ? p[2 * i] * (__uint_as_float(dv[2 * i]) - Dh) * s.scale : 0.f;
           const float d1 = have ? p[2 * i + 1] * (__uint_as_float(dv[2 * i + 1]) - Dh) * s.scale : 0.f;
-          split_bf16x2(p[2 * i], p[2 * i + 1], reinterpret_cast<uint32_t*>(ph)[i],
-                       reinterpret_cast<uint32_t*>(pl)[i]);
-          split_bf16x2(d0, d1, reinterpret_cast<uint32_t*>(dh)[i], reinterpret_cast<uint32_t*>(dl)[i]);
+          split_bf16x2(p[2 * i], p[2 * i + 1], pk[0][i], pk[1][i]);
+          split_bf16x2(d0, d1, pk[2][i], pk[3][i]);
         }
-        const long long o = rh * k + slot0 + cc;
-        uint4* o_ph = reinterpret_cast<uint4*>(P_ws + o);
-        uint4* o_pl = reinterpret_cast<uint4*>(Plo_ws + o);
-        uint4* o_dh = reinterpret_cast<uint4*>(dS_ws + o);
-        uint4* o_dl = reinterpret_cast<uint4*>(dSlo_ws + o);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (slot0 + cc + 8 * i < k) {  // k is a multiple of 8
-            o_ph[i] = ph[i];
-            o_pl[i] = pl[i];
-            o_dh[i] = dh[i];
-            o_dl[i] = dl[i];
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             smem_u32(stg + (a * kH + h) * kPitch + 16 * i)),
+                         "r"(pk[a][4 * i]), "r"(pk[a][4 * i + 1]), "r"(pk[a][4 * i + 2]),
+                         "r"(pk[a][4 * i + 3]) : "memory");
+      }
+      if (colsum) {
+        // sum p over this warp's 32 heads for each of the 32 keys (recursive
+        // halving: lane L ends with key L's sum), in a fixed order
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const bool up = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < o; ++i) {
+            const float send = up ? p[i] : p[i + o];
+            const float keep = up ? p[i + o] : p[i];
+            p[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
           }
         }
+        psum[quad * kSTile + cc + lane] = p[0];
       }
-      if (!kGrad || praw) {
-        // transpose through shared memory, [key][head] with a 129-float row
-        // pitch (conflict-free writes by head and reads by key); the kv tile
-        // is no longer needed once the MMAs are done
+      if (kGrad) {
+        named_bar_sync(1, 128);  // the chunk is staged
+        const int piece = t & 3;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) T[(cc + i) * (kH + 1) + h] = p[i];
+        for (int r = 0; r < 16; ++r) {  // 4 arrays x 128 rows x 4 pieces of 16 bytes
+          const int a = r >> 2, hh = ((t >> 2) + 32 * r) & 127;
+          __nv_bfloat16* arr = a == 0 ? P_ws : a == 1 ? Plo_ws : a == 2 ? dS_ws : dSlo_ws;
+          if (slot0 + cc + 8 * piece < k) {  // k is a multiple of 8
+            const uint4 v4 = *reinterpret_cast<const uint4*>(stg + (a * kH + hh) * kPitch + 16 * piece);
+            *reinterpret_cast<uint4*>(arr + (row * kH + hh) * (long long)k + slot0 + cc + 8 * piece) = v4;
+          }
+        }
+        named_bar_sync(1, 128);  // before the next chunk overwrites the staging
       }
     }
-    if (!kGrad || praw) {
+    if (colsum) {
       named_bar_sync(1, 128);
-      const int key = h;  // thread = key: sum its row over the 128 heads
-      float acc = 0.f;
-      for (int hh = 0; hh < kH; ++hh) acc += T[key * (kH + 1) + hh];
+      const int key = t;  // thread = key: the four quadrants' sums in a fixed order
+      const float acc = ((psum[key] + psum[kSTile + key]) + psum[2 * kSTile + key]) + psum[3 * kSTile + key];
       if (slot0 + key < k) praw[row * k + slot0 + key] = acc;
     }
   }
