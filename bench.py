@@ -420,32 +420,77 @@ def main():
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h = sum(t.numel() * t.element_size() for t in host_out.values())
 
+        # The step is cut into row chunks (dsa_forward with q_row_offset, as a
+        # context-parallel shard would call it) so that the host->device copy
+        # of chunk c+1 and the device->host copy of chunk c-1 overlap the
+        # compute of chunk c on three streams.  Rows are independent, so the
+        # results equal one whole-sequence call bit for bit.
+        nch = 8 if S % 32 == 0 else 1
+        R = S // nch
+        s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+        pc = [mk(q_row_offset=c * R, **{}) for c in range(nch)]
+        for c in range(nch):
+            pc[c].S_q = R
+        rows = lambda t, c: t[:, c * R:(c + 1) * R]
+        prev = {"cmp": None, "out": [None] * nch}
+
         def e2e_step():
-            for n in host_in:
-                x[n].copy_(host_in[n], non_blocking=True)
-            dsa.forward(p, x["q_I"], x["k_I"], x["w"], x["q"], x["kv"], idx, out, m, l, ring)
-            host_out["idx"].copy_(idx, non_blocking=True)
-            host_out["out"].copy_(out, non_blocking=True)
-            host_out["m"].copy_(m, non_blocking=True)
-            host_out["l"].copy_(l, non_blocking=True)
+            e_kv, e_in, e_done, e_out = E(), [E() for _ in range(nch)], [E() for _ in range(nch)], \
+                [E() for _ in range(nch)]
+            with torch.cuda.stream(s_in):
+                if prev["cmp"] is not None:     # the previous step no longer reads the inputs
+                    s_in.wait_event(prev["cmp"])
+                x["k_I"].copy_(host_in["k_I"], non_blocking=True)
+                x["kv"].copy_(host_in["kv"], non_blocking=True)
+                e_kv.record(s_in)
+                for c in range(nch):
+                    for n in ("q_I", "w", "q"):
+                        rows(x[n], c).copy_(rows(host_in[n], c), non_blocking=True)
+                    e_in[c].record(s_in)
+            s_cmp.wait_event(e_kv)
+            for c in range(nch):
+                s_cmp.wait_event(e_in[c])
+                if prev["out"][c] is not None:  # the previous step's outputs are copied out
+                    s_cmp.wait_event(prev["out"][c])
+                dsa.forward(pc[c], rows(x["q_I"], c), x["k_I"], rows(x["w"], c), rows(x["q"], c),
+                            x["kv"], rows(idx, c), rows(out, c), rows(m, c), rows(l, c), ring,
+                            stream=s_cmp)
+                e_done[c].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                for c in range(nch):
+                    s_out.wait_event(e_done[c])
+                    for n, t in (("idx", idx), ("out", out), ("m", m), ("l", l)):
+                        rows(host_out[n], c).copy_(rows(t, c), non_blocking=True)
+                    e_out[c].record(s_out)
+            prev["cmp"], prev["out"] = e_done[-1], e_out
+            return e_out[-1]
 
         for _ in range(2):
             e2e_step()
         torch.cuda.synchronize()
         ke = max(3, K // 2)
         a, b = E(), E()
-        a.record(stream)
+        a.record(s_in)
         for _ in range(ke):
-            e2e_step()
-        b.record(stream)
+            last = e2e_step()
+        s_out.wait_event(last)
+        b.record(s_out)
         torch.cuda.synchronize()
         ms_e2e = a.elapsed_time(b) / ke
         if world > 1:
             tt = torch.tensor([ms_e2e], device=dev)
             torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
             ms_e2e = float(tt)
+        # the chunked path returns what one whole-sequence call returns
+        ref = dict(idx=torch.empty_like(idx), out=torch.empty_like(out), m=torch.empty_like(m),
+                   l=torch.empty_like(l))
+        dsa.forward(p, x["q_I"], x["k_I"], x["w"], x["q"], x["kv"], ref["idx"], ref["out"],
+                    ref["m"], ref["l"], ring)
+        torch.cuda.synchronize()
+        same = all(torch.equal(ref[n].cpu(), host_out[n]) for n in ref)
         e2e = {"value": world * S / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "row_chunks": nch,
+               "equals_whole_call": same}
         assert dsa.get_status() == 0
 
     bwd = None
