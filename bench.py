@@ -53,6 +53,26 @@ def load_peaks():
     return d
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: every rank's step time, all-reduced with MAX
+    (the job's time is its slowest replica's)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t)
+
+
+def job_value(world: int, rows_per_rank: int, ms: float) -> float:
+    """Whole-job throughput: the query rows all ranks processed / the job's time."""
+    return world * rows_per_rank / (ms * 1e-3)
+
+
+def replica_seed(rank: int) -> int:
+    """Each rank draws its own replica problem (weak scaling)."""
+    return rank
+
+
 def algorithmic(wl, pos):
     """Work the method must do (causal / selected pairs only)."""
     n = pos.astype(np.float64) + 1.0
@@ -336,7 +356,7 @@ def main():
         return
 
     S, k = wl["S"], wl["topk"]
-    x = synth.make_inputs(wl, device=dev, seed=rank)   # each rank: its own replica problem
+    x = synth.make_inputs(wl, device=dev, seed=replica_seed(rank))  # each rank: its own replica
     mk = lambda **kw: dsa.make_params(B=1, S_q=S, S_k=S, H=wl["H"], d_qk=wl["d_qk"], d_v=wl["d_v"],
                                       H_I=wl["H_I"], d_I=wl["d_I"], topk=k, scale=wl["scale"],
                                       dtype="bf16", **kw)
@@ -396,15 +416,12 @@ def main():
     K = args.steps
     t_idx, t_topk, t_attn = t_idx / K, t_topk / K, t_attn / K      # ms per step
     ms_step = t_idx + t_topk + t_attn
-    if world > 1:
-        tt = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(tt)
+    ms_step = max_over_ranks(ms_step, world, dev)
 
     f_idx, f_attn, topk_bytes = algorithmic(wl, np.arange(S))
     peaks = load_peaks()
     peak_tc = peaks["bf16_tflops_sustained"]
-    value = world * S / (ms_step * 1e-3)
+    value = job_value(world, S, ms_step)
     attn_tflops = f_attn / (t_attn * 1e-3) / 1e12
     tensor_frac = (f_idx + f_attn) / ((t_idx + t_attn) * 1e-3) / 1e12 / peak_tc
 
@@ -477,10 +494,7 @@ def main():
         b.record(s_out)
         torch.cuda.synchronize()
         ms_e2e = a.elapsed_time(b) / ke
-        if world > 1:
-            tt = torch.tensor([ms_e2e], device=dev)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            ms_e2e = float(tt)
+        ms_e2e = max_over_ranks(ms_e2e, world, dev)
         # the chunked path returns what one whole-sequence call returns
         ref = dict(idx=torch.empty_like(idx), out=torch.empty_like(out), m=torch.empty_like(m),
                    l=torch.empty_like(l))
@@ -488,7 +502,7 @@ def main():
                     ref["m"], ref["l"], ring)
         torch.cuda.synchronize()
         same = all(torch.equal(ref[n].cpu(), host_out[n]) for n in ref)
-        e2e = {"value": world * S / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_value(world, S, ms_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "row_chunks": nch,
                "equals_whole_call": same}
         assert dsa.get_status() == 0
