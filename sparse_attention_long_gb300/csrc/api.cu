@@ -101,6 +101,21 @@ bool make_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 rows of `ld` floats viewed as [rows][lines][32]: line l of row r holds
+// columns [32l, 32l + 32); boxes of box_lines lines with the 128-byte swizzle
+bool make_tmap_f32_lines(CUtensorMap* tm, const float* base, uint64_t rows, uint64_t ld,
+                         uint64_t lines, uint32_t box_lines) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {32, lines, rows};
+  cuuint64_t strides[2] = {128, ld * 4};
+  cuuint32_t box[3] = {32, box_lines, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------ validation ---------------------------------
 static bool aligned16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
 

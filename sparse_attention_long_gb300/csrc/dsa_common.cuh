@@ -318,9 +318,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
 
 // order-preserving map of fp32 bits to uint32 (-0.0 first folded onto +0.0)
 __device__ __forceinline__ uint32_t ordered_key(float x) {
-  uint32_t u = __float_as_uint(x);
-  if ((u << 1) == 0u) u = 0u;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  // x + 0 turns -0 into +0 (IEEE round-to-nearest) and leaves every other
+  // value unchanged; then negative values get all bits flipped, others the sign
+  const uint32_t u = __float_as_uint(x + 0.0f);
+  return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
 }
 
 }  // namespace dsa

@@ -130,101 +130,319 @@ __device__ __forceinline__ void radix_select(TopkSmem& sm, int k, ForEach for_ea
   take_eq = k_rem;
 }
 
-template <int VEC>
-__global__ void __launch_bounds__(TK_THREADS, 1)
-    topk_reg_kernel(Shape s, const float* __restrict__ scores, long long ld, long long row_begin,
-                    int32_t* __restrict__ idx, DevCtx c) {
-  __shared__ TopkSmem sm;
-  const long long r_local = blockIdx.x;
-  const long long row = row_begin + r_local;
-  const int k = s.topk;
-  int32_t* out = idx + r_local * (long long)k;
-  const long long pos = row_pos(s, row);
-  if (pos < 0 || pos >= s.S_k) {
-    if (threadIdx.x == 0) set_status(c, DSA_ERR_INDEX);
-    write_prefix_rows(out, 0, k);
-    return;
-  }
-  const int n = (int)pos + 1;
-  if (n <= k) {
-    write_prefix_rows(out, n, k);
-    return;
-  }
-  const float* src = scores + r_local * ld;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int wbase = warp * 128 * VEC;
-  const bool vec_ok = ((reinterpret_cast<uintptr_t>(src) & 15u) == 0);
-  uint32_t key[VEC][4];
+// Register-resident variant: thread t holds the KPT consecutive scores
+// [t*KPT, t*KPT + KPT) of the row (positions past the row end read as key 0
+// and are masked out), so one block scan of per-thread counts gives every
+// winner its output slot in index order.  The later radix passes only touch
+// the keys whose prefix matched the previous pass; each pass has its own
+// histogram, all cleared at the start, and the threshold search takes two
+// barriers.
+constexpr int TK_CAND = 4096;
+struct TopkRegSmem {
+  uint32_t hist[2 * TK_HIST + 256];  // pass 1 | pass 2 | pass 3
+  uint32_t cand[TK_CAND];            // keys of the threshold's pass-1 bin
+  uint32_t ws[TK_WARPS];
+  uint32_t bin, above, bin_count;
+  int abort_flag;
+  unsigned long long bar;  // stage-full barrier (8-byte aligned by the layout)
+};
+
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x, int lane) {
 #pragma unroll
-  for (int j = 0; j < VEC; ++j) {
-    const int e0 = wbase + j * 128 + lane * 4;
-    if (vec_ok && e0 + 3 < n) {
-      float4 v = __ldcs(reinterpret_cast<const float4*>(src + e0));
-      key[j][0] = ordered_key(v.x);
-      key[j][1] = ordered_key(v.y);
-      key[j][2] = ordered_key(v.z);
-      key[j][3] = ordered_key(v.w);
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+
+// Exclusive scan of v over the block in thread order; one barrier.  ws must
+// not be written again before the next barrier every thread passes.
+__device__ __forceinline__ uint32_t block_excl_scan_1b(uint32_t v, uint32_t* ws) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t x = warp_incl_scan(v, lane);
+  if (lane == 31) ws[warp] = x;
+  __syncthreads();
+  const uint32_t t = ws[lane];
+  const uint32_t ti = warp_incl_scan(t, lane);
+  return __shfl_sync(0xffffffffu, ti - t, warp) + x - v;
+}
+
+// The bin b of hist[0..NB), counted from the top, with
+// count(> b) < k_rem <= count(>= b); result in sm.bin / above / bin_count.
+template <int NB>
+__device__ __forceinline__ void find_bin_2b(TopkRegSmem& sm, const uint32_t* hist, uint32_t k_rem) {
+  constexpr int PER = NB >= TK_THREADS ? NB / TK_THREADS : 1;
+  static_assert(PER == 1 || PER == 4, "bins per thread");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int hi = NB - (int)threadIdx.x * PER;  // this thread: bins [hi-PER, hi)
+  uint32_t h[PER];  // h[j] = count of bin hi-1-j
+  if constexpr (PER == 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(hist + hi - 4);
+    h[0] = v.w;
+    h[1] = v.z;
+    h[2] = v.y;
+    h[3] = v.x;
+  } else {
+    h[0] = hi > 0 ? hist[hi - 1] : 0u;
+  }
+  uint32_t local = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) local += h[j];
+  const uint32_t x = warp_incl_scan(local, lane);
+  if (lane == 31) sm.ws[warp] = x;
+  if (threadIdx.x == 0) sm.bin = 0, sm.above = 0, sm.bin_count = 0;
+  __syncthreads();
+  const uint32_t t = sm.ws[lane];
+  const uint32_t ti = warp_incl_scan(t, lane);
+  uint32_t acc = __shfl_sync(0xffffffffu, ti - t, warp) + x - local;
+  if (acc < k_rem && acc + local >= k_rem) {
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      if (acc < k_rem && acc + h[j] >= k_rem) {
+        sm.bin = (uint32_t)(hi - 1 - j);
+        sm.above = acc;
+        sm.bin_count = h[j];
+      }
+      acc += h[j];
+    }
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int x, int y, int z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(tm), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+// (mask << 1) | (a > b), given nb = ~b: a + ~b carries out exactly when a > b.
+__device__ __forceinline__ uint32_t shift_in_gt(uint32_t mask, uint32_t a, uint32_t nb) {
+  uint32_t r;
+  asm("{\n .reg .u32 t;\n add.cc.u32 t, %1, %2;\n addc.u32 %0, %3, %3;\n}"
+      : "=r"(r)
+      : "r"(a), "r"(nb), "r"(mask));
+  return r;
+}
+
+// Persistent: CTA b takes rows b, b + gridDim.x, ...  When the scores are
+// reachable by TMA (tma_elems > 0: the first tma_elems columns of every row,
+// viewed as 128-byte lines) one thread loads the CTA's next row into a
+// shared-memory stage as soon as the current one has been read from it, so
+// the next row streams in while this one is selected.  The 128-byte swizzle
+// puts 16-byte piece g of a row at g ^ ((g >> 3) & 7), so the 8 lanes of a
+// quarter-warp reading their consecutive pieces hit distinct banks.
+template <int KPT>
+__global__ void __launch_bounds__(TK_THREADS, 1)
+    topk_reg_kernel(const __grid_constant__ CUtensorMap tm, Shape s, const float* __restrict__ scores,
+                    long long ld, long long row_begin, long long rows, int32_t* __restrict__ idx,
+                    DevCtx c, int tma_elems) {
+  static_assert(KPT % 4 == 0 && KPT <= 32, "keys per thread");
+  constexpr int C = KPT / 4;                          // 16-byte pieces per thread
+  constexpr int BOX_ROWS = 32 * KPT < 256 ? 32 * KPT : 256;  // 128-byte lines per TMA box
+  constexpr int BOX_ELEMS = BOX_ROWS * 32;
+  extern __shared__ uint8_t dyn_smem[];  // [align 1024] stage | TopkRegSmem
+  const uint32_t base = smem_u32(dyn_smem);
+  uint8_t* aligned = dyn_smem + (((base + 1023u) & ~1023u) - base);
+  const float4* stage = reinterpret_cast<const float4*>(aligned);
+  TopkRegSmem& sm = *reinterpret_cast<TopkRegSmem*>(aligned + TK_THREADS * KPT * 4);
+  volatile int* abort_flag = &sm.abort_flag;
+  const uint32_t bar = smem_u32(&sm.bar), stage_u32 = smem_u32(aligned);
+  const int k = s.topk;
+  const int e0 = threadIdx.x * KPT;  // this thread's first element of a row
+  const bool staged = tma_elems > 0 && e0 + KPT <= tma_elems;  // my keys come from the stage
+  auto row_len = [&](long long rl) -> long long {  // n = pos + 1, or -1 for a bad position
+    const long long pos = row_pos(s, row_begin + rl);
+    return (pos < 0 || pos >= s.S_k) ? -1 : pos + 1;
+  };
+  auto loads_row = [&](long long rl) { return tma_elems > 0 && rl < rows && row_len(rl) > k; };
+  auto issue = [&](long long rl) {  // thread 0: stage row rl if it is selected from
+    if (threadIdx.x != 0 || !loads_row(rl)) return;
+    const int nn = (int)row_len(rl);
+    const int nbox = (min(nn, tma_elems) + BOX_ELEMS - 1) / BOX_ELEMS;
+    fence_proxy_async_smem();  // the stage's earlier reads come before these writes
+    mbar_arrive_expect_tx(bar, (uint32_t)(nbox * BOX_ELEMS * 4));
+    for (int bx = 0; bx < nbox; ++bx)
+      tma_load_3d(stage_u32 + bx * BOX_ELEMS * 4, &tm, 0, bx * BOX_ROWS, (int)rl, bar);
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  uint32_t phase = 0;
+  issue(blockIdx.x);
+  for (long long rl = blockIdx.x; rl < rows; rl += gridDim.x) {
+    int32_t* out = idx + rl * (long long)k;
+    const long long nl = row_len(rl);
+    if (nl < 0) {
+      if (threadIdx.x == 0) set_status(c, DSA_ERR_INDEX);
+      write_prefix_rows(out, 0, k);
+      issue(rl + gridDim.x);
+      continue;
+    }
+    if (nl <= k) {
+      write_prefix_rows(out, (int)nl, k);
+      issue(rl + gridDim.x);
+      continue;
+    }
+    const int n = (int)nl;
+    const int nv = min(max(n - e0, 0), KPT);
+    const uint32_t vmask = nv >= 32 ? 0xFFFFFFFFu : ((1u << nv) - 1u);
+    const float* src = scores + rl * ld;
+    uint32_t key[KPT];
+    bool ok = true;
+    if (tma_elems > 0) {
+      ok = mbar_wait(bar, phase, c, abort_flag);
+      phase ^= 1u;
+    }
+    if (staged) {
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        const int g = threadIdx.x * C + j;
+        const float4 v = stage[g ^ ((g >> 3) & 7)];
+        key[4 * j] = ordered_key(v.x);
+        key[4 * j + 1] = ordered_key(v.y);
+        key[4 * j + 2] = ordered_key(v.z);
+        key[4 * j + 3] = ordered_key(v.w);
+      }
+      if (nv < KPT) {
+#pragma unroll
+        for (int q = 0; q < KPT; ++q)
+          if (q >= nv) key[q] = 0u;
+      }
     } else {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) key[j][q] = (e0 + q < n) ? ordered_key(__ldcs(src + e0 + q)) : 0u;
+      for (int q = 0; q < KPT; ++q) key[q] = q < nv ? ordered_key(__ldcs(src + e0 + q)) : 0u;
     }
-  }
-  auto for_each = [&](auto fn) {
+    for (int i = threadIdx.x; i < 2 * TK_HIST + 256; i += TK_THREADS) sm.hist[i] = 0;
+    if (__syncthreads_or(!ok)) return;  // a stage load that never landed: give up
+    // pass 1: bits 31..20 of every key
+    uint32_t* h1 = sm.hist;
+    if (nv == KPT) {
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) {
-      const int e0 = wbase + j * 128 + lane * 4;
+      for (int q = 0; q < KPT; ++q) atomicAdd(&h1[key[q] >> 20], 1u);
+    } else {
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (e0 + q < n) fn(key[j][q]);
+      for (int q = 0; q < KPT; ++q)
+        if (q < nv) atomicAdd(&h1[key[q] >> 20], 1u);
     }
-  };
-  int sh;
-  uint32_t tp, take_eq;
-  radix_select(sm, k, for_each, sh, tp, take_eq);
-
-  // index-ordered compaction: packed (gt | eq << 16) counts
-  uint32_t pre[VEC];
-  uint32_t run = 0;
+    __syncthreads();
+    find_bin_2b<TK_HIST>(sm, h1, (uint32_t)k);
+    uint32_t k_rem = (uint32_t)k - sm.above;
+    const uint32_t b1 = sm.bin, c1 = sm.bin_count;
+    // keys above bin b1 (all taken) and keys in it, as bit masks over q
+    const uint32_t lo1 = b1 << 20, hi1 = lo1 | 0xFFFFFu;
+    uint32_t gtm = 0, eqm = 0;  // shifted in from q = 0 (ends in bit KPT-1), reversed below
 #pragma unroll
-  for (int j = 0; j < VEC; ++j) {
-    const int e0 = wbase + j * 128 + lane * 4;
-    uint32_t cnt = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (e0 + q < n) {
-        const uint32_t kk = key[j][q] >> sh;
-        cnt += (kk > tp) ? 1u : ((kk == tp) ? 0x10000u : 0u);
+    for (int q = 0; q < KPT; ++q) {
+      gtm = shift_in_gt(gtm, key[q], ~hi1);
+      eqm = shift_in_gt(eqm, key[q], ~(lo1 - 1u));  // key >= lo1 (when lo1 > 0)
+    }
+    if (lo1 == 0) eqm = 0xFFFFFFFFu;
+    gtm = (__brev(gtm) >> (32 - KPT)) & vmask;
+    eqm = (__brev(eqm) >> (32 - KPT)) & ~gtm & vmask;
+    if (c1 != k_rem && c1 <= (uint32_t)TK_CAND) {
+      // the c1 keys of bin b1 go to shared memory (in index order) and the
+      // later passes run over them alone
+      uint32_t off = block_excl_scan_1b((uint32_t)__popc(eqm), sm.ws);
+      for (uint32_t m = eqm; m; m &= m - 1u) {
+        const int q = __ffs(m) - 1;
+        const int g = threadIdx.x * C + (q >> 2);
+        const float v = staged ? reinterpret_cast<const float*>(stage + (g ^ ((g >> 3) & 7)))[q & 3]
+                               : src[e0 + q];
+        sm.cand[off++] = ordered_key(v);
       }
-    }
-    uint32_t x = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    pre[j] = run + x - cnt;
-    run += __shfl_sync(0xffffffffu, x, 31);
-  }
-  uint32_t total;
-  const uint32_t wexcl = block_scan_excl<uint32_t>(lane == 0 ? run : 0u, sm.warp_sum, &sm.total, total);
-  const uint32_t wbase_cnt = __shfl_sync(0xffffffffu, wexcl, 0);
-#pragma unroll
-  for (int j = 0; j < VEC; ++j) {
-    const int e0 = wbase + j * 128 + lane * 4;
-    uint32_t p = wbase_cnt + pre[j];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (e0 + q < n) {
-        const uint32_t kk = key[j][q] >> sh;
-        const uint32_t gt_b = p & 0xFFFFu, eq_b = p >> 16;
-        if (kk > tp) {
-          const uint32_t o = gt_b + min(eq_b, take_eq);
-          if (o < (uint32_t)k) out[o] = e0 + q;
-          p += 1u;
-        } else if (kk == tp) {
-          if (eq_b < take_eq && gt_b + eq_b < (uint32_t)k) out[gt_b + eq_b] = e0 + q;
-          p += 0x10000u;
+      __syncthreads();  // candidates complete; the stage is free
+      issue(rl + gridDim.x);
+      uint32_t* h2 = sm.hist + TK_HIST;
+      for (uint32_t i = threadIdx.x; i < c1; i += TK_THREADS)
+        atomicAdd(&h2[(sm.cand[i] >> 8) & 0xFFFu], 1u);
+      __syncthreads();
+      find_bin_2b<TK_HIST>(sm, h2, k_rem);
+      k_rem -= sm.above;
+      uint32_t tp = (b1 << 12) | sm.bin;
+      int sh = 8;
+      if (sm.bin_count != k_rem) {
+        uint32_t* h3 = sm.hist + 2 * TK_HIST;
+        const uint32_t b2 = sm.bin;
+        for (uint32_t i = threadIdx.x; i < c1; i += TK_THREADS) {
+          const uint32_t kk = sm.cand[i];
+          if (((kk >> 8) & 0xFFFu) == b2) atomicAdd(&h3[kk & 0xFFu], 1u);
         }
+        __syncthreads();
+        find_bin_2b<256>(sm, h3, k_rem);
+        k_rem -= sm.above;
+        sh = 0;
+        tp = (tp << 8) | sm.bin;
+      }
+      // classify this thread's candidates against the final threshold
+      const uint32_t tmin = tp << sh, tmax = tmin | ((1u << sh) - 1u);
+      uint32_t i = off - (uint32_t)__popc(eqm), cgt = 0, ceq = 0;
+      for (uint32_t m = eqm; m; m &= m - 1u, ++i) {
+        const uint32_t kk = sm.cand[i], bit = m & (0u - m);
+        if (kk > tmax)
+          cgt |= bit;
+        else if (kk >= tmin)
+          ceq |= bit;
+      }
+      gtm |= cgt;
+      eqm = ceq;
+    } else if (c1 != k_rem) {
+      // more than TK_CAND keys share the bin (heavy ties): passes over registers
+      issue(rl + gridDim.x);
+      uint32_t tp = b1;
+      int sh = 20;
+      uint32_t* h2 = sm.hist + TK_HIST;
+#pragma unroll
+      for (int q = 0; q < KPT; ++q)
+        if (q < nv && key[q] - lo1 < (1u << 20)) atomicAdd(&h2[(key[q] >> 8) & 0xFFFu], 1u);
+      __syncthreads();
+      find_bin_2b<TK_HIST>(sm, h2, k_rem);
+      k_rem -= sm.above;
+      sh = 8;
+      tp = (tp << 12) | sm.bin;
+      if (sm.bin_count != k_rem) {
+        uint32_t* h3 = sm.hist + 2 * TK_HIST;
+        const uint32_t lo2 = tp << 8;
+#pragma unroll
+        for (int q = 0; q < KPT; ++q)
+          if (q < nv && key[q] - lo2 < 256u) atomicAdd(&h3[key[q] & 0xFFu], 1u);
+        __syncthreads();
+        find_bin_2b<256>(sm, h3, k_rem);
+        k_rem -= sm.above;
+        sh = 0;
+        tp = (tp << 8) | sm.bin;
+      }
+      const uint32_t tmin = tp << sh, tmax = tmin | ((1u << sh) - 1u);
+      uint32_t cgt = 0, ceq = 0;
+#pragma unroll
+      for (int q = 0; q < KPT; ++q) {
+        cgt |= (key[q] > tmax ? 1u : 0u) << q;
+        ceq |= (key[q] >= tmin ? 1u : 0u) << q;
+      }
+      gtm = cgt & vmask;
+      eqm = ceq & ~cgt & vmask;
+    } else {
+      issue(rl + gridDim.x);  // every key of bin b1 is taken
+    }
+    const uint32_t take_eq = k_rem;
+    const uint32_t p =
+        block_excl_scan_1b((uint32_t)__popc(gtm) | ((uint32_t)__popc(eqm) << 16), sm.ws);
+    uint32_t gt_b = p & 0xFFFFu, eq_b = p >> 16;
+    for (uint32_t m = gtm | eqm; m; m &= m - 1u) {
+      const int q = __ffs(m) - 1;
+      if ((gtm >> q) & 1u) {
+        const uint32_t o = gt_b + min(eq_b, take_eq);
+        if (o < (uint32_t)k) out[o] = e0 + q;
+        ++gt_b;
+      } else {
+        if (eq_b < take_eq && gt_b + eq_b < (uint32_t)k) out[gt_b + eq_b] = e0 + q;
+        ++eq_b;
       }
     }
   }
@@ -289,21 +507,50 @@ __global__ void __launch_bounds__(TK_THREADS, 1)
   }
 }
 
+bool make_tmap_f32_lines(CUtensorMap* tm, const float* base, uint64_t rows, uint64_t ld,
+                         uint64_t lines, uint32_t box_lines);
+
 int launch_topk(const Shape& s, const float* scores, long long ld, long long row_begin,
                 long long rows, int32_t* idx, DevCtx c, cudaStream_t st) {
-  const int g = (int)rows;
+  if (rows <= 0) return DSA_OK;
   const int max_n = s.S_k;
-  if (max_n <= 4096)
-    topk_reg_kernel<1><<<g, TK_THREADS, 0, st>>>(s, scores, ld, row_begin, idx, c);
-  else if (max_n <= 8192)
-    topk_reg_kernel<2><<<g, TK_THREADS, 0, st>>>(s, scores, ld, row_begin, idx, c);
-  else if (max_n <= 16384)
-    topk_reg_kernel<4><<<g, TK_THREADS, 0, st>>>(s, scores, ld, row_begin, idx, c);
-  else if (max_n <= 32768)
-    topk_reg_kernel<8><<<g, TK_THREADS, 0, st>>>(s, scores, ld, row_begin, idx, c);
-  else
-    topk_stream_kernel<<<g, TK_THREADS, 0, st>>>(s, scores, ld, row_begin, idx, c);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  if (max_n > 32768) {
+    topk_stream_kernel<<<(int)rows, TK_THREADS, 0, st>>>(s, scores, ld, row_begin, idx, c);
+    return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  }
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+      return DSA_ERR_CUDA;
+  }
+  const int g = (int)(rows < sms ? rows : sms);
+  const int kpt = max_n <= 4096 ? 4 : max_n <= 8192 ? 8 : max_n <= 16384 ? 16 : 32;
+  // TMA view of each row: S_k / 32 lines of 32 floats (the last S_k % 32
+  // columns, if any, are read directly)
+  CUtensorMap tm;
+  memset(&tm, 0, sizeof(tm));
+  int tma_elems = 0;
+  if ((reinterpret_cast<uintptr_t>(scores) & 15u) == 0 && ld % 4 == 0 && max_n >= 32) {
+    const uint32_t box_lines = 32 * kpt < 256 ? 32 * kpt : 256;
+    if (!make_tmap_f32_lines(&tm, scores, (uint64_t)rows, (uint64_t)ld, (uint64_t)(max_n / 32),
+                             box_lines))
+      return DSA_ERR_CUDA;
+    tma_elems = (max_n / 32) * 32;
+  }
+  const size_t smem = 1024 + (size_t)TK_THREADS * kpt * 4 + sizeof(TopkRegSmem);
+  auto run = [&](auto kernel) -> int {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return DSA_ERR_CUDA;
+    kernel<<<g, TK_THREADS, smem, st>>>(tm, s, scores, ld, row_begin, rows, idx, c, tma_elems);
+    return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  };
+  if (kpt == 4) return run(topk_reg_kernel<4>);
+  if (kpt == 8) return run(topk_reg_kernel<8>);
+  if (kpt == 16) return run(topk_reg_kernel<16>);
+  return run(topk_reg_kernel<32>);
 }
 
 }  // namespace dsa

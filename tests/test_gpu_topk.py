@@ -51,10 +51,11 @@ def test_ties_and_signed_zero(k):
     _check(dsa, sc, np.arange(S), k)
 
 
-@pytest.mark.parametrize("S_k,k,rows", [(1001, 100, 200), (4096, 2048, 512), (32768, 2048, 96),
+@pytest.mark.parametrize("S_k,k,rows", [(1001, 100, 200), (4096, 2048, 512), (32768, 2048, 320),
                                         (40000, 2048, 24)])
 def test_random_rows(S_k, k, rows):
-    # 4096..32768: register-resident rows; 40000: streaming variant; 1001: rows
+    # 4096..32768: register-resident rows (more rows than SMs, so CTAs take
+    # several rows each); 40000: streaming variant; 1001: rows
     # not 16-byte aligned (scalar loads)
     dsa = lib()
     sc = synth.normal((rows, S_k), 7, seed=1, dtype=torch.float32).numpy() * 8.0
