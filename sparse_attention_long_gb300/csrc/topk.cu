@@ -254,8 +254,12 @@ __global__ void __launch_bounds__(TK_THREADS, 1)
   const int k = s.topk;
   const int e0 = threadIdx.x * KPT;  // this thread's first element of a row
   const bool staged = tma_elems > 0 && e0 + KPT <= tma_elems;  // my keys come from the stage
+  // 32-bit row -> position arithmetic when it fits (a 64-bit modulo is slow)
+  const bool narrow = s.q_row_index == nullptr && row_begin + rows <= 0x7FFFFFFFll;
   auto row_len = [&](long long rl) -> long long {  // n = pos + 1, or -1 for a bad position
-    const long long pos = row_pos(s, row_begin + rl);
+    const long long pos =
+        narrow ? s.q_row_offset + (long long)((uint32_t)(row_begin + rl) % (uint32_t)s.S_q)
+               : row_pos(s, row_begin + rl);
     return (pos < 0 || pos >= s.S_k) ? -1 : pos + 1;
   };
   auto loads_row = [&](long long rl) { return tma_elems > 0 && rl < rows && row_len(rl) > k; };
