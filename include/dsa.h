@@ -95,7 +95,9 @@ typedef struct {
   int32_t reserved1;
   int64_t q_row_offset;        /* global position of local row 0 (if no q_row_index)  */
   const int32_t *q_row_index;  /* optional device [B*S_q] global positions, or NULL   */
-  int64_t wave_rows;           /* dsa_forward: rows per indexer/top-k wave; 0 = auto  */
+  int64_t wave_rows;           /* dsa_forward: rows per indexer/top-k wave; 0 = auto:
+                                  as many as fit 256 MB of scores, rounded down to a
+                                  multiple of 4 x the SM count (at least 1024) */
 } dsa_params;
 
 /* Library version as 10000*major + 100*minor + patch. */

@@ -111,13 +111,9 @@ def make_params(*, B, S_q, S_k, H, d_qk, d_v, H_I, d_I, topk, scale, dtype="bf16
 
 
 def wave_rows(p: dsa_params) -> int:
-    """Rows per indexer/top-k wave dsa_forward uses (mirrors the library)."""
-    total = p.B * p.S_q
-    w = p.wave_rows
-    if w <= 0:
-        w = max((256 << 20) // (4 * p.S_k), 1024)
-    w = (w + 3) // 4 * 4
-    return min(w, total)
+    """Rows per indexer/top-k wave dsa_forward uses: its score ring holds one
+    wave of S_k fp32 scores per row, so the library's workspace size gives it."""
+    return workspace_size(p, DSA_CALL_FORWARD) // (4 * p.S_k)
 
 
 def version() -> int:
