@@ -11,8 +11,9 @@
 // columns [512+32c, 512+32c+32) -- 288 of the 576 contraction columns and
 // half of O.  Per 64-key block each CTA
 //   1. gathers its 288 columns of the 64 selected kv rows into swizzled shared
-//      memory (four producer warps; each warp-wide 16-byte load covers one
-//      key's contiguous 512-byte latent half, so every load is coalesced),
+//      memory (four producer warps issuing cp.async copies, several blocks in
+//      flight; each warp-wide 16-byte copy covers one key's contiguous
+//      512-byte latent half, so every access is coalesced),
 //   2. computes the partial logits S_c = Q_c K_c^T (M=128 heads, N=64, K=288)
 //      into one of three TMEM logit buffers,
 //   3. swaps S_c with its peer through distributed shared memory: four
@@ -88,6 +89,16 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+
+// 16-byte global -> shared copy that bypasses registers (L2 only)
+__device__ __forceinline__ void cp_async16_cg(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// arrive on `bar` once every cp.async this thread issued before has landed
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // D[tmem] (+)= A[tmem] * B[smem]^T
 __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
@@ -180,49 +191,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp >= kWarpGather0 && warp < kWarpX0) {
     // ------------------------------- kv gather -------------------------------
     // warp gw owns keys gw, gw+4, ..., gw+60 of every block.  Latent half: one
-    // warp-wide 16-byte load per key (lane = 16-byte chunk of the 512 bytes);
-    // rope quarter: 8 keys x 4 chunks per load.  Stores follow the SW128 (latent,
-    // 64 columns per 128-byte row) and SW64 (rope, 32 columns) K-major layouts.
+    // warp-wide 16-byte copy per key (lane = 16-byte chunk of the 512 bytes);
+    // rope quarter: 8 keys x 4 chunks per copy.  The copies go straight to
+    // shared memory (cp.async, no register staging), in the SW128 (latent, 64
+    // columns per 128-byte row) and SW64 (rope, 32 columns) K-major layouts, so
+    // a warp keeps issuing the next blocks while earlier ones are in flight:
+    // up to kStages blocks of the gather overlap.
     const int gw = warp - kWarpGather0;
     const __nv_bfloat16* kvb = reinterpret_cast<const __nv_bfloat16*>(kvg) + b * s.S_k * (long long)kDQK;
     const int lat_col = 256 * (int)crank + 8 * lane;               // this lane's latent chunk
     const int rope_m = lane >> 2, rope_c = lane & 3;
     const int rope_col = 512 + 32 * (int)crank + 8 * rope_c;
+    const int g = lane >> 3, cc = lane & 7;
     for (int j = 0; j < nblk; ++j) {
       const int st = j % kStages;
       if (!mbar_wait_warp(smem_u32(&sm.kv_empty[st]), ((j / kStages) & 1) ^ 1, c, abort_flag)) break;
-      uint4 lat[16], rope[2];
+      const uint32_t kvs = smem_u32(sm.kv[st]);
 #pragma unroll
       for (int m = 0; m < 16; ++m) {
         const int e = j * kBKey + gw + 4 * m;
         const int id = e < k ? sm.idx[e] : -1;
-        lat[m] = __ldg(reinterpret_cast<const uint4*>(kvb + (long long)(id < 0 ? 0 : id) * kDQK + lat_col));
+        const int r = gw + 4 * m;
+        cp_async16_cg(kvs + g * kKVChunk + r * 128 + ((cc ^ (r & 7)) << 4),
+                      kvb + (long long)(id < 0 ? 0 : id) * kDQK + lat_col);
       }
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int e = j * kBKey + gw + 4 * (8 * i + rope_m);
         const int id = e < k ? sm.idx[e] : -1;
-        rope[i] = __ldg(reinterpret_cast<const uint4*>(kvb + (long long)(id < 0 ? 0 : id) * kDQK + rope_col));
-      }
-      const uint32_t kvs = smem_u32(sm.kv[st]);
-      const int g = lane >> 3, cc = lane & 7;
-#pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        const int r = gw + 4 * m;
-        const uint32_t dst = kvs + g * kKVChunk + r * 128 + ((cc ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(lat[m].x),
-                     "r"(lat[m].y), "r"(lat[m].z), "r"(lat[m].w) : "memory");
-      }
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
         const int r = gw + 4 * (8 * i + rope_m);
-        const uint32_t dst = kvs + 4 * kKVChunk + r * 64 + ((rope_c ^ ((r >> 1) & 3)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(rope[i].x),
-                     "r"(rope[i].y), "r"(rope[i].z), "r"(rope[i].w) : "memory");
+        cp_async16_cg(kvs + 4 * kKVChunk + r * 64 + ((rope_c ^ ((r >> 1) & 3)) << 4),
+                      kvb + (long long)(id < 0 ? 0 : id) * kDQK + rope_col);
       }
-      fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor cores
-      mbar_arrive(smem_u32(&sm.kv_full[st]));
+      // kv_full completes once all 128 gather threads' copies of this block
+      // have landed; the MMA issuer fences them into the async proxy
+      cp_async_arrive_noinc(smem_u32(&sm.kv_full[st]));
     }
+    cp_async_wait_all();  // no copy may still be in flight when the CTA exits
     if (warp == kWarpGather0 && lane == 0) mbar_wait(smem_u32(&sm.q_full), 0, c, abort_flag);
   } else if (warp == kWarpMMA) {
     // ------------------------------- MMA issuer -------------------------------
@@ -242,6 +247,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int st = ns % kStages, sb = ns % kSBuf;
           if (mbar_test(smem_u32(&sm.kv_full[st]), (ns / kStages) & 1) &&
               mbar_test(smem_u32(&sm.s_free[sb]), ((ns / kSBuf) & 1) ^ 1)) {
+            fence_proxy_async_smem();  // the gathered tile (cp.async writes) -> tensor cores
             tc_fence_after();
             const uint32_t kv0 = smem_u32(sm.kv[st]);
             const uint32_t d = tmem + kColS + sb * kBKey;
