@@ -439,16 +439,31 @@ def main():
 
         # The step is cut into row chunks (dsa_forward with q_row_offset, as a
         # context-parallel shard would call it) so that the host->device copy
-        # of chunk c+1 and the device->host copy of chunk c-1 overlap the
-        # compute of chunk c on three streams.  Rows are independent, so the
-        # results equal one whole-sequence call bit for bit.
-        nch = 8 if S % 32 == 0 else 1
-        R = S // nch
+        # of the next chunk and the device->host copy of the previous one
+        # overlap the compute of the current chunk on three streams.  Rows are
+        # independent, so the results equal one whole-sequence call bit for
+        # bit.  Chunks run from the last rows to the first: causal rows get
+        # cheaper towards the start while their copies do not, so the heavy
+        # chunks hide the copies of the light ones; the first and last chunks
+        # are small so that the copy-in before the first compute and the
+        # copy-out after the last one are short.
+        if S % 4096 == 0 and S >= 16384:
+            sizes = [1024, 3072] + [4096] * (S // 4096 - 2) + [3072, 1024]
+        else:
+            sizes = [S]
+        bounds = []
+        r1 = S
+        for n_rows in sizes:                 # descending rows
+            bounds.append((r1 - n_rows, r1))
+            r1 -= n_rows
+        nch = len(bounds)
         s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
-        pc = [mk(q_row_offset=c * R, **{}) for c in range(nch)]
-        for c in range(nch):
-            pc[c].S_q = R
-        rows = lambda t, c: t[:, c * R:(c + 1) * R]
+        pc = []
+        for (r0, r1) in bounds:
+            pr = mk(q_row_offset=r0)
+            pr.S_q = r1 - r0
+            pc.append(pr)
+        rows = lambda t, c: t[:, bounds[c][0]:bounds[c][1]]
         prev = {"cmp": None, "out": [None] * nch}
 
         def e2e_step():
