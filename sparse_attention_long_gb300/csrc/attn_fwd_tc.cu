@@ -9,12 +9,16 @@
 // TMEM columns of an SM, leaving nothing for the logits.  So the two CTAs of a
 // cluster split the columns: CTA c owns V columns [256c, 256c+256) and rope
 // columns [512+32c, 512+32c+32) -- 288 of the 576 contraction columns and
-// half of O.  Per 64-key block each CTA
+// half of O.  TMEM per CTA: O half [0,256), three logit/P buffers
+// [256,448), and the first 128 of the query half's 256 latent columns
+// [448,512) as the A operand of the logit MMA -- which frees the shared
+// memory for a fourth kv stage.  Per 64-key block each CTA
 //   1. gathers its 288 columns of the 64 selected kv rows into swizzled shared
-//      memory (four producer warps issuing cp.async copies, several blocks in
-//      flight; each warp-wide 16-byte copy covers one key's contiguous
+//      memory (four producer warps issuing cp.async copies, up to four blocks
+//      in flight; each warp-wide 16-byte copy covers one key's contiguous
 //      512-byte latent half, so every access is coalesced),
-//   2. computes the partial logits S_c = Q_c K_c^T (M=128 heads, N=64, K=288)
+//   2. computes the partial logits S_c = Q_c K_c^T (M=128 heads, N=64, K=288:
+//      latent columns 0..127 with A in TMEM, the rest from shared memory)
 //      into one of three TMEM logit buffers,
 //   3. swaps S_c with its peer through distributed shared memory: four
 //      exchange warps send each block as soon as its logits are in TMEM
@@ -33,8 +37,9 @@
 // in shared memory once, so no global load sits on the per-block path.
 //
 // Roles per CTA: warp 0 = TMEM owner + MMA issuer, warps 1..4 = kv gather (warp 1
-// also TMA-loads the query half), warps 5..8 = logit exchange and sum, warps
-// 9..12 = softmax / epilogue (one warp per TMEM lane quadrant, thread = head).
+// also TMA-loads the shared-memory part of the query), warps 5..8 = logit
+// exchange and sum, warps 9..12 = query columns into TMEM, then softmax /
+// epilogue (one warp per TMEM lane quadrant, thread = head).
 #include <math.h>
 
 #include "dsa_common.cuh"
@@ -46,11 +51,12 @@ constexpr int kH = 128, kDQK = 576, kDV = 512;
 constexpr int kBKey = 64;                         // keys per block
 constexpr int kMaxTopk = 2048;                    // index row staged in shared memory
 constexpr int kMaxBlk = kMaxTopk / kBKey;
-constexpr int kStages = 3;                        // KV gather stages
+constexpr int kStages = 4;                        // KV gather stages
 constexpr int kSBuf = 3;                          // TMEM logit / P buffers
 constexpr int kQChunk = kH * 128;                 // 64 cols x 128 heads (SW128)
 constexpr int kQRope = kH * 64;                   // 32 cols x 128 heads (SW64)
-constexpr int kQBytes = 4 * kQChunk + kQRope;     // 72 KB
+constexpr int kQTmemDims = 128;                   // latent cols 0..127 of the half: A in TMEM
+constexpr int kQBytes = 2 * kQChunk + kQRope;     // latent cols 128..255 + rope: 40 KB
 constexpr int kKVChunk = kBKey * 128;             // 8 KB
 constexpr int kKVRope = kBKey * 64;               // 4 KB
 constexpr int kKVStage = 4 * kKVChunk + kKVRope;  // 36 KB
@@ -62,6 +68,8 @@ constexpr int kWarpMMA = 0, kWarpGather0 = 1, kWarpX0 = kWarpGather0 + kGatherWa
 constexpr int kThreads = 32 * (1 + kGatherWarps + kXWarps + kSoftWarps);
 constexpr int kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256;        // O: [0,256)  logits/P: 256 + 64*b
+constexpr uint32_t kColQ = kColS + kSBuf * kBKey;  // query latent cols 0..127 (bf16 pairs)
+static_assert(kColQ + kQTmemDims / 2 <= 512, "TMEM columns");
 constexpr uint32_t kIdescS = idesc_bf16(128, kBKey, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
@@ -74,7 +82,7 @@ struct __align__(1024) Smem {
   float x[kH * kBKey];                            // peer's partial logits [16 x 4-key chunk][head][4]
   int32_t idx[kMaxTopk];                          // the token's index row (-1 = skip)
   unsigned long long mask[kMaxBlk];               // per 64-slot block: valid slots
-  uint64_t q_full, kv_full[kStages], kv_empty[kStages], s_full[kSBuf], s_free[kSBuf],
+  uint64_t q_full, q_tm, kv_full[kStages], kv_empty[kStages], s_full[kSBuf], s_free[kSBuf],
       c_full[kSBuf], p_full[kSBuf], x_full, x_free, mma_done;
   uint32_t tmem_base;
   int abort;
@@ -100,6 +108,19 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// Non-blocking phase test (mbarrier.test_wait never suspends the thread,
+// unlike try_wait), for the MMA issuer's loop over several conditions.
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]^T
 __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
@@ -112,7 +133,8 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qr,
-                       const void* __restrict__ kvg, Shape s, const int32_t* __restrict__ idx,
+                       const void* __restrict__ qg, const void* __restrict__ kvg, Shape s,
+                       const int32_t* __restrict__ idx,
                        __nv_bfloat16* __restrict__ out,
                        float* __restrict__ mx, float* __restrict__ sm_out, long long nrows,
                        DevCtx c) {
@@ -130,6 +152,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 32 * kWarpGather0) {
     mbar_init(smem_u32(&sm.q_full), 1);
+    mbar_init(smem_u32(&sm.q_tm), kSoftWarps * 32);  // query cols 0..127 stored into TMEM
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&sm.kv_full[i]), kGatherWarps * 32);
       mbar_init(smem_u32(&sm.kv_empty[i]), 1);
@@ -153,9 +176,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t qb = smem_u32(&sm.q_full);
     mbar_arrive_expect_tx(qb, kQBytes);
     const int qrow = (int)(row * kH);
-    for (int i = 0; i < 4; ++i)
-      tma_load_2d(q0 + i * kQChunk, &tm_q, (int)(256 * crank + 64 * i), qrow, qb);
-    tma_load_2d(q0 + 4 * kQChunk, &tm_qr, (int)(512 + 32 * crank), qrow, qb);
+    for (int i = 0; i < 2; ++i)
+      tma_load_2d(q0 + i * kQChunk, &tm_q, (int)(256 * crank + kQTmemDims + 64 * i), qrow, qb);
+    tma_load_2d(q0 + 2 * kQChunk, &tm_qr, (int)(512 + 32 * crank), qrow, qb);
   }
   if (warp == kWarpMMA) {
     tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
@@ -234,33 +257,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0 && nblk > 0) {
       // Issue whichever is ready: the logits S(ns) of the next block (needs its
       // gathered tile and a free logit buffer, i.e. PV(ns-3) done) or PV(np) of
-      // the oldest block whose P is written.  S runs at most one block ahead of
-      // the PVs issued so far (letting it run two ahead produced rare
-      // run-to-run differences in a few rows; see the design notes).
-      bool ok = mbar_wait(smem_u32(&sm.q_full), 0, c, abort_flag);
+      // the oldest block whose P is written.  S runs up to two blocks ahead of
+      // the next PV.  The readiness tests do not block (test_wait), so a PV
+      // whose P is written is never held up by a wait on a later tile.
+      bool ok = mbar_wait(smem_u32(&sm.q_full), 0, c, abort_flag) &&
+                mbar_wait(smem_u32(&sm.q_tm), 0, c, abort_flag);
       int ns = 0, np = 0;
       uint64_t t_idle = 0;
       uint32_t spins = 0;
       while (ok && np < nblk) {
         bool progressed = false;
-        if (ns < nblk && ns < np + 2) {
+        if (ns < nblk && ns < np + 3) {
           const int st = ns % kStages, sb = ns % kSBuf;
-          if (mbar_test(smem_u32(&sm.kv_full[st]), (ns / kStages) & 1) &&
-              mbar_test(smem_u32(&sm.s_free[sb]), ((ns / kSBuf) & 1) ^ 1)) {
+          if (mbar_poll(smem_u32(&sm.kv_full[st]), (ns / kStages) & 1) &&
+              mbar_poll(smem_u32(&sm.s_free[sb]), ((ns / kSBuf) & 1) ^ 1)) {
             fence_proxy_async_smem();  // the gathered tile (cp.async writes) -> tensor cores
             tc_fence_after();
             const uint32_t kv0 = smem_u32(sm.kv[st]);
             const uint32_t d = tmem + kColS + sb * kBKey;
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
+            for (int kk = 0; kk < kQTmemDims / 16; ++kk) {  // latent cols 0..127: A in TMEM
+              const uint64_t bd = sdesc(kv0 + (kk >> 2) * kKVChunk + (kk & 3) * 32, 16, 1024, kSw128);
+              mma_bf16_ts(d, tmem + kColQ + kk * 8, bd, kIdescS, kk > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int kk = kQTmemDims / 16; kk < 16; ++kk) {  // latent cols 128..255: A in shared memory
               const uint32_t off = (kk & 3) * 32;
-              const uint64_t ad = sdesc(q0 + (kk >> 2) * kQChunk + off, 16, 1024, kSw128);
+              const uint64_t ad = sdesc(q0 + ((kk - kQTmemDims / 16) >> 2) * kQChunk + off, 16, 1024, kSw128);
               const uint64_t bd = sdesc(kv0 + (kk >> 2) * kKVChunk + off, 16, 1024, kSw128);
-              mma_bf16_ss(d, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+              mma_bf16_ss(d, ad, bd, kIdescS, 1u);
             }
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
-              const uint64_t ad = sdesc(q0 + 4 * kQChunk + kk * 32, 16, 512, kSw64);
+              const uint64_t ad = sdesc(q0 + 2 * kQChunk + kk * 32, 16, 512, kSw64);
               const uint64_t bd = sdesc(kv0 + 4 * kKVChunk + kk * 32, 16, 512, kSw64);
               mma_bf16_ss(d, ad, bd, kIdescS, 1u);
             }
@@ -271,7 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (np < ns) {
           const int st = np % kStages, sb = np % kSBuf;
-          if (mbar_test(smem_u32(&sm.p_full[sb]), (np / kSBuf) & 1)) {
+          if (mbar_poll(smem_u32(&sm.p_full[sb]), (np / kSBuf) & 1)) {
             tc_fence_after();
             const uint32_t kv0 = smem_u32(sm.kv[st]);
             const uint32_t pa = tmem + kColS + sb * kBKey;
@@ -374,6 +403,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const float sl2e = s.scale * kLog2e;
     float m_run = -INFINITY, m_true = -INFINITY, l_run = 0.f;
+    {
+      // The query's latent cols 0..127 of this half: 256 contiguous bytes per
+      // head, into TMEM as the A operand of the logit MMA (column i holds
+      // elements 2i, 2i+1).
+      const uint4* src = reinterpret_cast<const uint4*>(
+          reinterpret_cast<const __nv_bfloat16*>(qg) + (row * kH + h) * (long long)kDQK + 256 * crank);
+#pragma unroll 1
+      for (int cc = 0; cc < kQTmemDims / 64; ++cc) {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v4 = __ldg(src + 8 * cc + i);
+          w[4 * i] = v4.x;
+          w[4 * i + 1] = v4.y;
+          w[4 * i + 2] = v4.z;
+          w[4 * i + 3] = v4.w;
+        }
+        tmem_st32(tmem + lane_off + kColQ + 32 * cc, w);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.q_tm));
+    }
     // A failed (timed-out) wait turns the rest of this warp's work into no-ops.
     bool ok = true;
     for (int j = 0; ok && j < nblk; ++j) {
@@ -502,7 +554,7 @@ int launch_attn_fwd_tc(const Shape& s, const void* q, const void* kv, const int3
     return DSA_ERR_CUDA;
   const long long nrows = (long long)s.B * s.S_q;
   attn_fwd_tc_kernel<<<(unsigned)(2 * nrows), kThreads, smem, st>>>(
-      tq, tqr, kv, s, idx, (__nv_bfloat16*)out, mx, sm, nrows, c);
+      tq, tqr, q, kv, s, idx, (__nv_bfloat16*)out, mx, sm, nrows, c);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
