@@ -26,6 +26,16 @@
 namespace dsa {
 namespace bwd {
 
+// 16-byte global -> shared copy that bypasses registers (L2 only)
+__device__ __forceinline__ void cp_async16_cg(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// arrive on `bar` once every cp.async this thread issued before has landed
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 constexpr int kH = 128, kDQK = 576, kDV = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -167,25 +177,21 @@ __global__ void __launch_bounds__(kSThreads, 2)
       for (int i = 0; i < nC; ++i) {
         const int st = i % kSStages;
         if (!mbar_wait_warp(smem_u32(&sm.empty[st]), ((i / kSStages) & 1) ^ 1, c, abort_flag)) break;
-        uint4 r[8];
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const int key = (t >> 3) + 16 * m;
-          const int id = sm.idx[key] < 0 ? 0 : sm.idx[key];
-          r[m] = __ldg(reinterpret_cast<const uint4*>(kvb + (long long)id * kDQK + 64 * i) + cc);
-        }
+        // straight into the swizzled stage (cp.async): the next chunks are
+        // issued while this one is in flight; full[st] counts this thread's
+        // arrive once its copies have landed, and the MMA issuer fences them
+        // into the async proxy
         const uint32_t kvs = smem_u32(sm.st[st][0]);
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
           const int key = (t >> 3) + 16 * m;
-          const uint32_t dst = kvs + key * 128 + ((cc ^ (key & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(r[m].x),
-                       "r"(r[m].y), "r"(r[m].z), "r"(r[m].w)
-                       : "memory");
+          const int id = sm.idx[key] < 0 ? 0 : sm.idx[key];
+          cp_async16_cg(kvs + key * 128 + ((cc ^ (key & 7)) << 4),
+                        reinterpret_cast<const uint4*>(kvb + (long long)id * kDQK + 64 * i) + cc);
         }
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&sm.full[st]));
+        cp_async_arrive_noinc(smem_u32(&sm.full[st]));
       }
+      cp_async_wait_all();  // no copy may still be in flight when the CTA exits
     } else if (lane == 0) {
       // MMA: S (TMEM cols 0..127) and dP (cols 128..255), M=128 heads, N=128 keys
       constexpr uint32_t idesc = idesc_bf16(128, kSTile, false, false);
@@ -194,6 +200,7 @@ __global__ void __launch_bounds__(kSThreads, 2)
         const int st = i % kSStages;
         ok = mbar_wait(smem_u32(&sm.full[st]), (i / kSStages) & 1, c, abort_flag);
         if (!ok) break;
+        fence_proxy_async_smem();  // the gathered kv chunk (cp.async writes) -> tensor cores
         tc_fence_after();
         const uint32_t kv0 = smem_u32(sm.st[st][0]), q0 = smem_u32(sm.st[st][1]),
                        o0 = smem_u32(sm.st[st][2]);
@@ -393,34 +400,28 @@ __global__ void __launch_bounds__(192, 1)
     for (int ch = 0; ch < nch; ++ch) {
       const int st = ch % kQStages;
       if (!mbar_wait_warp(smem_u32(&sm.empty[st]), ((ch / kQStages) & 1) ^ 1, c, abort_flag)) break;
-      uint4 r[16];
-#pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        const int key = gw + 4 * m;
-        const int sl = 64 * ch + key;
-        const int id = (sl < k && sm.idx[sl] >= 0) ? sm.idx[sl] : 0;
-        if (lane < 24) r[m] = __ldg(reinterpret_cast<const uint4*>(kvb + (long long)id * kDQK) + lane);
-      }
+      // straight into the swizzled stage (cp.async), as in the scores kernel
       const uint32_t bs = smem_u32(sm.bm[st]);
       if (lane < 24) {
         const int at = lane >> 3, cc = lane & 7;
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
           const int key = gw + 4 * m;
-          const uint32_t dst = bs + at * 8192 + key * 128 + ((cc ^ (key & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(r[m].x),
-                       "r"(r[m].y), "r"(r[m].z), "r"(r[m].w)
-                       : "memory");
+          const int sl = 64 * ch + key;
+          const int id = (sl < k && sm.idx[sl] >= 0) ? sm.idx[sl] : 0;
+          cp_async16_cg(bs + at * 8192 + key * 128 + ((cc ^ (key & 7)) << 4),
+                        reinterpret_cast<const uint4*>(kvb + (long long)id * kDQK) + lane);
         }
       }
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&sm.full[st]));
+      cp_async_arrive_noinc(smem_u32(&sm.full[st]));
     }
+    cp_async_wait_all();  // no copy may still be in flight when the CTA exits
   } else if (lane == 0) {
     constexpr uint32_t idesc = idesc_bf16(128, kQN, false, true);
     for (int ch = 0; ch < nch; ++ch) {
       const int st = ch % kQStages;
       if (!mbar_wait(smem_u32(&sm.full[st]), (ch / kQStages) & 1, c, abort_flag)) break;
+      fence_proxy_async_smem();  // the gathered kv rows (cp.async writes) -> tensor cores
       tc_fence_after();
       const uint32_t b0 = smem_u32(sm.bm[st]);
 #pragma unroll
