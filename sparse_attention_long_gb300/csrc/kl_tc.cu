@@ -29,6 +29,16 @@
 namespace dsa {
 namespace kltc {
 
+// 16-byte global -> shared copy that bypasses registers (L2 only)
+__device__ __forceinline__ void cp_async16_cg(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// arrive on `bar` once every cp.async this thread issued before has landed
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 constexpr int kHI = 64, kDI = 128, kTile = 128, kMaxK = 2048;
 constexpr int kThreads = 160;
 constexpr uint32_t kColS = 0, kColDK = 64, kColDQ = 192;   // TMEM columns
@@ -46,7 +56,7 @@ struct __align__(1024) Smem {
   float wv[kHI];
   float dws[4][kHI];            // per-warp dw partials (summed in a fixed order)
   float red[8];
-  uint64_t kt_full, s_done, ds_full, g_done;
+  uint64_t kt_full, s_done, s_free, ds_full, g_done;
   uint32_t tmem_base;
   int abort;
   int last;
@@ -99,6 +109,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sm.kt_full), 128);
     mbar_init(smem_u32(&sm.s_done), 1);
+    mbar_init(smem_u32(&sm.s_free), 128);  // pass A: the workers have read S^T
     mbar_init(smem_u32(&sm.ds_full), 128);
     mbar_init(smem_u32(&sm.g_done), 1);
     sm.abort = 0;
@@ -136,7 +147,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       bool ok = true;
       for (int it = 0; ok && it < 2 * ntile; ++it) {
         ok = mbar_wait(smem_u32(&sm.kt_full), it & 1, c, abort_flag);
+        // the previous S^T must have been read before this one overwrites it
+        // (in pass B the wait for dS below orders that already)
+        if (ok && it >= 1 && it <= ntile)
+          ok = mbar_wait(smem_u32(&sm.s_free), (it - 1) & 1, c, abort_flag);
         if (!ok) break;
+        fence_proxy_async_smem();  // the gathered key tile (cp.async writes) -> tensor cores
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)   // S^T = K_tile q_I^T over the 128 dims
@@ -191,20 +207,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     psum = workers_sum(psum, sm.red);
     const float pinv = psum > 0.f ? 1.f / psum : 0.f;
     for (int i = t; i < k; i += 128) sm.pv[i] *= pinv;
-    auto gather = [&](int tile) {  // k_I rows of the tile's 128 slots, swizzled K-major
+    // k_I rows of the tile's 128 slots, swizzled K-major, copied straight to
+    // shared memory (cp.async); kt_full counts each worker's arrive once its
+    // copies have landed.  A tile's gather is issued as soon as the key tile
+    // is free (the MMAs that read it have completed), so it overlaps the
+    // workers' processing of the previous tile.
+    auto gather = [&](int tile) {
       const int cch = t & 15;
 #pragma unroll 4
       for (int i = 0; i < 16; ++i) {
         const int key = (t >> 4) + 8 * i;
         const int sl = tile * kTile + key;
         const int id = (sl < k && sm.idx[sl] >= 0) ? sm.idx[sl] : 0;
-        const uint4 v4 = __ldg(reinterpret_cast<const uint4*>(kIb + (long long)id * kDI) + cch);
-        const uint32_t dst = kt0 + (cch >> 3) * (kTile * 128) + key * 128 + (((cch & 7) ^ (key & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v4.x), "r"(v4.y),
-                     "r"(v4.z), "r"(v4.w) : "memory");
+        cp_async16_cg(kt0 + (cch >> 3) * (kTile * 128) + key * 128 + (((cch & 7) ^ (key & 7)) << 4),
+                      reinterpret_cast<const uint4*>(kIb + (long long)id * kDI) + cch);
       }
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&sm.kt_full));
+      cp_async_arrive_noinc(smem_u32(&sm.kt_full));
     };
     auto load_s = [&](uint32_t (&s0)[32], uint32_t (&s1)[32]) {
       tmem_ld32(tmem + lane_off + kColS, s0);
@@ -214,14 +232,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     };
     int n_s = 0;  // S^T commits consumed so far
     // ---- pass A: indexer logits ----
+    if (ok) gather(0);
     for (int tile = 0; ok && tile < ntile; ++tile) {
-      gather(tile);
       ok = mbar_wait_warp(smem_u32(&sm.s_done), n_s & 1, c, abort_flag);
       ++n_s;
       if (!ok) break;
       tc_fence_after();
       uint32_t s0[32], s1[32];
       load_s(s0, s1);
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.s_free));
+      gather(tile + 1 < ntile ? tile + 1 : 0);  // the last one: pass B's first tile
       const int sl = tile * kTile + my;
       float I = -INFINITY;
       if (sl < k && sm.idx[sl] >= 0) {
@@ -264,7 +285,6 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int j = 0; j < kHI; ++j) dwp[j] = 0.f;
     for (int tile = 0; ok && tile < ntile; ++tile) {
-      gather(tile);
       ok = mbar_wait_warp(smem_u32(&sm.s_done), n_s & 1, c, abort_flag);
       ++n_s;
       if (!ok) break;
@@ -301,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       ok = mbar_wait_warp(smem_u32(&sm.g_done), tile & 1, c, abort_flag);
       if (!ok) break;
       tc_fence_after();
+      if (tile + 1 < ntile) gather(tile + 1);  // the key tile is free once dq^T is done
       // scatter this key's dk_I row
       const int id = valid ? sm.idx[sl] : -1;
       float* dst = dk_I + (b * s.S_k + (id < 0 ? 0 : id)) * (long long)kDI;
@@ -318,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       tc_fence_before();
     }
+    cp_async_wait_all();  // no copy may still be in flight when the CTA exits
     // ---- dq_I (thread = dim) and dw ----
     {
       uint32_t q0[32], q1[32];
