@@ -223,13 +223,10 @@ int launch_indexer_tc(const Shape& s, const void* q_I, const void* k_I, const vo
   if (!make_tmap_2d_bf16(&tq, q_I, (uint64_t)s.B * s.S_q * kHI, kDI, 64, kN, 128)) return DSA_ERR_CUDA;
   if (!make_tmap_2d_bf16(&tk, k_I, (uint64_t)s.B * s.S_k, kDI, 64, kBK, 128)) return DSA_ERR_CUDA;
   const size_t smem = sizeof(Smem) + 1024;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return DSA_ERR_CUDA;
-    attr_done = true;
-  }
+  // per call: the attribute belongs to the current device's context
+  if (cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return DSA_ERR_CUDA;
   const long long r_end = row_begin + rows;
   for (int b = 0; b < s.B; ++b) {
     const long long lo = row_begin > (long long)b * s.S_q ? row_begin : (long long)b * s.S_q;

@@ -522,13 +522,10 @@ int launch_topk(const Shape& s, const float* scores, long long ld, long long row
     topk_stream_kernel<<<(int)rows, TK_THREADS, 0, st>>>(s, scores, ld, row_begin, idx, c);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
   }
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
-      return DSA_ERR_CUDA;
-  }
+  int dev = 0, sms = 0;  // the current device's SM count (queried per call: devices may differ)
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return DSA_ERR_CUDA;
   const int g = (int)(rows < sms ? rows : sms);
   const int kpt = max_n <= 4096 ? 4 : max_n <= 8192 ? 8 : max_n <= 16384 ? 16 : 32;
   // TMA view of each row: S_k / 32 lines of 32 floats (the last S_k % 32
