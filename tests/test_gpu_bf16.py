@@ -199,3 +199,27 @@ def test_forward_c3_full_size_sampled_rows():
     assert ok, (ma, mr)
     assert np.abs(np64(o["m"])[0, rows] - m[0]).max() < 1e-4
     assert (np.abs(np64(o["l"])[0, rows] - l[0]) / l[0]).max() < 1e-4
+
+
+@pytest.mark.parametrize("S,k", [(1, 1), (5, 4), (37, 16), (130, 64)])
+def test_forward_tiny_sequences(S, k):
+    # fewer keys than one 64-key block, a single selected key, k >= n for most
+    # rows: the pipelines run one (partial) block per token
+    dsa = lib()
+    wl = _wl(S, k)
+    x = synth.make_inputs(wl)
+    sc, ridx, O, m, l = oracle.dsa_forward(x["q_I"], x["k_I"], x["w"], x["q"], x["kv"], k,
+                                           wl["scale"], wl["d_v"])
+    p = params(dsa, wl)
+    o = empty_outputs(wl, S, torch.bfloat16)
+    ws = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_FORWARD) // 4 + 4, device=DEV)
+    g = {n: v.to(DEV) for n, v in x.items()}
+    dsa.forward(p, g["q_I"], g["k_I"], g["w"], g["q"], g["kv"], o["idx"], o["out"], o["m"], o["l"], ws)
+    torch.cuda.synchronize()
+    assert dsa.get_status() == 0
+    gi = o["idx"].cpu().numpy()
+    assert near_tie_violations(gi[0], ridx[0], sc[0], k) == []
+    same = np.all(gi == ridx, axis=2)
+    ok, ma, mr = bf16_close(np64(o["out"])[same], O[same])
+    assert ok, (ma, mr)
+    assert np.abs(np64(o["m"])[same] - m[same]).max() < 1e-4
