@@ -130,7 +130,9 @@ int dsa_indexer_scores(const dsa_params *p, const void *q_I, const void *k_I, co
  * idx[(r - row_begin)*topk ...] in ascending index order; when
  * pos(t)+1 < topk the tail is -1.  Bit-exact (integer compares on an
  * order-preserving map of the fp32 bits).  NaN scores: unspecified order.
- *   scores [rows, S_k] fp32 (only s <= pos(t) are read)   idx [rows, topk] int32
+ *   scores [rows, S_k] fp32 (values at s > pos(t) are ignored; the buffer must
+ *          hold all rows x S_k floats: whole 128-byte lines of a row may be read)
+ *   idx [rows, topk] int32
  */
 int dsa_topk(const dsa_params *p, const float *scores, int64_t row_begin, int64_t rows,
              int32_t *idx, dsa_stream_t stream);
