@@ -97,7 +97,8 @@ typedef struct {
   const int32_t *q_row_index;  /* optional device [B*S_q] global positions, or NULL   */
   int64_t wave_rows;           /* dsa_forward: rows per indexer/top-k wave; 0 = auto:
                                   as many as fit 256 MB of scores, rounded down to a
-                                  multiple of 4 x the SM count (at least 1024) */
+                                  multiple of 4 x the SM count; 1024 when not even
+                                  that many fit */
 } dsa_params;
 
 /* Library version as 10000*major + 100*minor + patch. */

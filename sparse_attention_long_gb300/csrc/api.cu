@@ -194,19 +194,21 @@ static bool tc_bwd_shape(const dsa_params* p) {
 
 // Rows per indexer / top-k wave.  Auto: as many as fit a 256 MB score ring,
 // rounded down to a whole number of indexer rounds (4 rows per CTA, one CTA
-// per SM), so that no round of a wave runs with idle SMs; at least 1024.
+// per SM), so that no round of a wave runs with idle SMs; when not even one
+// round fits (very long rows), 1024 rows.
 static long long wave_rows(const dsa_params* p) {
   const long long total = p->B * p->S_q;
   long long w = p->wave_rows;
   if (w <= 0) {
     w = (256ll << 20) / (4 * p->S_k);
     int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0) {
-      const long long round_rows = 4ll * sms;
-      if (w >= round_rows) w = w / round_rows * round_rows;
-    }
-    if (w < 1024) w = 1024;
+    const long long round_rows =
+        (cudaGetDevice(&dev) == cudaSuccess &&
+         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+            ? 4ll * sms
+            : 1024;
+    if (w >= round_rows) w = w / round_rows * round_rows;
+    else if (w < 1024) w = 1024;
   }
   w = (w + 3) / 4 * 4;
   return w < total ? w : total;

@@ -72,3 +72,23 @@ def test_bf16_batch2_attention_against_oracle():
     ok, ma, mr = bf16_close(np64(o["out"]), O)
     assert ok, (ma, mr)
     assert np.abs(np64(o["m"]) - m).max() < 1e-4
+
+
+def test_auto_wave_is_whole_indexer_rounds():
+    # the forward's score ring holds one wave; its auto size is a multiple of
+    # 4 rows x the SM count (one four-row indexer CTA per SM per round) when
+    # the 256 MB budget allows it, the whole call when that is shorter, and
+    # 1024 rows when not even one round fits
+    dsa = lib()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for S in (4096, 16384, 32768, 65536, 131072):
+        wl = dict(synth.v32(S, f"dsv32_S{S}"))
+        p = params(dsa, wl)
+        w = dsa.wave_rows(p)
+        budget = (256 << 20) // (4 * S)
+        if budget >= S:
+            assert w == S
+        elif budget >= 4 * sms:
+            assert w % (4 * sms) == 0 and w <= budget and w + 4 * sms > budget, (S, w)
+        else:
+            assert w == 1024
