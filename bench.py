@@ -408,11 +408,14 @@ def main():
     assert dsa.get_status() == 0, "device status after the timed steps"
 
     t_idx = t_topk = t_attn = 0.0
+    per_step = []                       # ms of each timed step (for the median)
     for e in evs:
+        t0 = t_idx + t_topk + t_attn
         for i in range(len(waves)):
             t_idx += e["idx"][i][0].elapsed_time(e["idx"][i][1])
             t_topk += e["idx"][i][1].elapsed_time(e["topk"][i][1])
         t_attn += e["attn"][0].elapsed_time(e["attn"][1])
+        per_step.append(t_idx + t_topk + t_attn - t0)
     K = args.steps
     t_idx, t_topk, t_attn = t_idx / K, t_topk / K, t_attn / K      # ms per step
     ms_step = t_idx + t_topk + t_attn
@@ -538,7 +541,8 @@ def main():
     traffic = kernel_traffic("attn_fwd_tc.cu", "attn_fwd_tc_dsv32.md")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_step,
+        "ms_per_step_median": float(np.median(per_step)), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl["name"], "B": 1, "S": S, "topk": k, "H": wl["H"],
                    "d_qk": wl["d_qk"], "d_v": wl["d_v"], "H_I": wl["H_I"], "d_I": wl["d_I"],
