@@ -111,3 +111,19 @@ def test_kl_finite_differences():
             fm = f()
             arr[i] = old
             assert abs((fp - fm) / (2 * eps) - grad[i]) < 1e-7, i
+
+
+def test_kl_logit_gradient_sums_to_zero():
+    # dI = Softmax(I) - p sums to 0 over a token's selected keys (both are
+    # distributions).  Seen through dw: an index head whose score is the same
+    # positive constant c for every key adds c to all logits, so its weight's
+    # gradient is c * sum_i dI_i = 0, whatever the other heads do.
+    q, kv, idx, m, l, scale, qI, kI, w = _kl_case(17)
+    qI = qI.copy()
+    kI = kI.copy()
+    qI[..., 0, :] = 0.0
+    qI[..., 0, 0] = 1.0                      # head 0: q_I = e_0 for every token
+    kI[..., 0] = 0.75                        # k_I[s, 0] = 0.75 for every key
+    _, _, _, dw = indexer_kl_loss(q, kv, idx, m, l, scale, qI, kI, w)
+    assert np.abs(dw[..., 0]).max() < 1e-14
+    assert np.abs(dw[..., 1:]).max() > 1e-6  # the other heads do get gradient
