@@ -96,6 +96,37 @@ def main():
         "expected_dk_I": [[[dI0], [0.0], [dI1]]],
     })
 
+    # Two attention heads whose softmax sums l differ, so the target p depends
+    # on normalising each head by its own l before the head sum.
+    q0, q1 = 3.0 / 8.0, 5.0 / 8.0
+    loss2 = q0 * math.log(q0 / pi0) + q1 * math.log(q1 / pi1)
+    dJ0, dJ1 = pi0 - q0, pi1 - q1
+    dump("kl_loss_hand_2heads.json", {
+        "cite": SRC + ": the target p sums the attention probabilities over all heads, then L1-normalises "
+                      "along the context; Loss = sum_t KL(p_t || Softmax(I_t)); dI = Softmax(I) - p",
+        "derivation": [
+            "attention part: H = 2, scale 1, selected keys 0 and 2 of the kv rows below",
+            "head 0: q = [0,0,1] -> logits [0, ln 3]; m = ln 3, l = 4/3; P = [1/4, 3/4]",
+            "head 1: q = [0,0,0] -> logits [0, 0]; m = 0, l = 2; P = [1/2, 1/2]",
+            "head sum [3/4, 5/4] over the total 2 -> p = [3/8, 5/8]",
+            "(without the per-head division by l the head sum of exp(s - m) is [4/3, 2] and p would be "
+            "[2/5, 3/5]; weighting heads by l gives yet another p)",
+            "indexer part as in kl_loss_hand.json: I = [1, 3] on keys 0, 2, pi = softmax(I)",
+            "loss = 3/8 ln((3/8)/pi0) + 5/8 ln((5/8)/pi1); dI = [pi0 - 3/8, pi1 - 5/8]",
+            "dw = dI0*1 + dI1*3; dq~ = dI0*1 + dI1*3; dk~[0] = dI0, dk~[2] = dI1, dk~[1] = 0"],
+        "scale": 1.0,
+        "q": [[[[0.0, 0.0, 1.0], [0.0, 0.0, 0.0]]]],
+        "kv": [kv],
+        "idx": [[[0, 2]]],
+        "m": [[[ln3, 0.0]]], "l": [[[4.0 / 3.0, 2.0]]],
+        "q_I": [[[[1.0]]]], "k_I": [[[1.0], [5.0], [3.0]]], "w": [[[1.0]]],
+        "expected_p": [q0, q1],
+        "expected_loss": loss2,
+        "expected_dw": [[[dJ0 + 3 * dJ1]]],
+        "expected_dq_I": [[[[dJ0 + 3 * dJ1]]]],
+        "expected_dk_I": [[[dJ0], [0.0], [dJ1]]],
+    })
+
 
 if __name__ == "__main__":
     main()

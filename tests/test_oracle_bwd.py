@@ -64,6 +64,25 @@ def test_kl_hand_example(golden):
     np.testing.assert_allclose(dk_I, a("expected_dk_I"), atol=1e-15)
 
 
+def test_kl_hand_example_two_heads(golden):
+    # two heads with different softmax sums l: the target is the head sum of
+    # each head's normalised probabilities (p = [3/8, 5/8] by hand)
+    g = golden("kl_loss_hand_2heads.json")
+    a = lambda n: np.array(g[n])
+    loss, dq_I, dk_I, dw = indexer_kl_loss(a("q"), a("kv"), a("idx"), a("m"), a("l"), g["scale"],
+                                           a("q_I"), a("k_I"), a("w"))
+    assert abs(loss - g["expected_loss"]) < 1e-14
+    np.testing.assert_allclose(dw, a("expected_dw"), atol=1e-15)
+    np.testing.assert_allclose(dq_I, a("expected_dq_I"), atol=1e-15)
+    np.testing.assert_allclose(dk_I, a("expected_dk_I"), atol=1e-15)
+    # the same m, l with the second head's sum doubled must change the loss
+    # (the target reads each head's own l)
+    l2 = a("l").copy()
+    l2[..., 1] *= 2.0
+    assert abs(indexer_kl_loss(a("q"), a("kv"), a("idx"), a("m"), l2, g["scale"], a("q_I"), a("k_I"),
+                               a("w"))[0] - g["expected_loss"]) > 1e-3
+
+
 def _kl_case(seed, S=14, H=3, d_qk=6, H_I=2, d_I=4, k=5, scale=0.5):
     rng = np.random.default_rng(seed)
     q = rng.standard_normal((1, S, H, d_qk))
