@@ -7,13 +7,15 @@ DEV = torch.device("cuda:0")
 # Agreement rules.  fp32 path: max-abs 1e-5.  bf16 path: max-abs 2e-2 and
 # mean-rel 2e-3 (sum|a-b| / sum|b|) against the fp64 oracle on the same
 # bf16-rounded inputs.  Indexer scores of the bf16 path are fp32 results of
-# exact bf16 products summed in fp32 (128 terms of magnitude <= ~40, then 64
-# weighted ReLUs): a few 1e-5 absolute, so they are held to max-abs 2e-3,
-# well inside the 1e-3-wide near-tie band used for end-to-end indices only
-# when summed errors stay below it.
+# exact bf16 products summed in fp32: 128 products of two unit normals per
+# index head (sum of magnitudes ~80, rounding ~80 * 2^-24 per add in the worst
+# order), then 64 ReLUs weighted by w ~ N(0, 1/64).  The measured error is a
+# few 1e-5; the bound below is about ten times that and half the 1e-3 band
+# inside which end-to-end index sets may differ (near ties), so a score error
+# can never by itself move a key across that band.
 FP32_TOL = 1e-5
 BF16_MAXABS, BF16_MEANREL = 2e-2, 2e-3
-SCORE_MAXABS = 2e-3
+SCORE_MAXABS = 5e-4
 NEAR_TIE = 1e-3
 
 

@@ -11,8 +11,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
-from gpu_util import DEV, lib, params
+from gpu_util import DEV, bf16_close, lib, np64, params
 
 pytestmark = pytest.mark.gpu
 
@@ -77,3 +78,16 @@ def test_head_tail_shards_sum_to_unsharded():
         err = (part[key].double() - ref).abs().max().item()
         assert err <= 1e-5 * max(ref.abs().max().item(), 1.0), (key, err)
     assert abs(part["loss"].item() - full["loss"].item()) <= 1e-5 * abs(full["loss"].item())
+    # and the shard sums equal the oracle's unsharded backward of the same
+    # forward results (idx, out, m, l), at the bf16 agreement rule
+    xc = {n: v.cpu() for n, v in x.items()}
+    gidx = idx.cpu().numpy()
+    Od, md, ld = np64(out), np64(m), np64(l)
+    _, dkv_r = oracle.sparse_attn_bwd(xc["q"], xc["kv"], gidx, Od, xc["dO"], md, ld, wl["scale"],
+                                      wl["d_v"])
+    loss_r, _, dkI_r, _ = oracle.indexer_kl_loss(xc["q"], xc["kv"], gidx, md, ld, wl["scale"],
+                                                 xc["q_I"], xc["k_I"], xc["w"])
+    for key, ref in (("dkv", dkv_r), ("dkI", dkI_r)):
+        ok, ma, mr = bf16_close(np64(part[key]), ref)
+        assert ok, (key, ma, mr)
+    assert abs(part["loss"].item() - loss_r) <= 1e-3 * abs(loss_r), (part["loss"].item(), loss_r)

@@ -64,11 +64,12 @@ def test_forward_end_to_end(case):
     torch.cuda.synchronize()
     gi = o["idx"].cpu().numpy()[0]
     assert near_tie_violations(gi, ref["idx"][0], ref["scores"][0], k) == []
-    same = [r for r in range(S) if set(gi[r]) == set(ref["idx"][0, r])]
-    assert len(same) > 0.9 * S
-    assert np.abs(np64(o["out"])[0, same] - ref["O"][0, same]).max() < FP32_TOL
-    # rows whose index sets match are exactly the oracle's rows; the other rows
-    # differ only by near-tied keys
+    # every row: the oracle's attention over the GPU's own index sets (equal
+    # to the oracle's own sets up to near-tied keys, checked above)
+    O, m, l = oracle.sparse_attn_fwd(x["q"], x["kv"], gi[None], WL["scale"], WL["d_v"])
+    assert np.abs(np64(o["out"]) - O).max() < FP32_TOL
+    assert np.abs(np64(o["m"]) - m).max() < FP32_TOL
+    assert np.abs(np64(o["l"]) - l).max() < FP32_TOL
 
 
 def test_cp_shards_bit_identical(case):
