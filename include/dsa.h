@@ -242,9 +242,10 @@ int dsa_forward(const dsa_params *p, const void *q_I, const void *k_I, const voi
  * allocator -- the score ring lives in a 32 MiB device array inside the
  * library, held on every GPU that loads the library until the process exits.
  * Arguments and outputs as dsa_forward; the waves hold as many rows as fit the
- * ring (a multiple of 4).  The ring's address is looked up on the first call
- * made on each device (make that call before any stream capture).  All calls
- * share the ring: calls that overlap on the GPU race on it.
+ * ring (a multiple of 4).  The ring's address is looked up by the first call
+ * made on each device (make that call before any stream capture) and again
+ * only if the device's CUDA context changed since.  All calls share the ring:
+ * calls that overlap on the GPU race on it.
  * Returns DSA_ERR_UNSUPPORTED when S_k > 2,097,152 (4 score rows would not
  * fit the ring); never allocates or frees device memory.
  */
@@ -257,6 +258,12 @@ int dsa_forward_static_ws(const dsa_params *p, const void *q_I, const void *k_I,
  * of the current device to *device_status (DSA_OK, DSA_ERR_TIMEOUT or
  * DSA_ERR_INDEX) and clears it.  Returns DSA_ERR_CUDA if the stream reported
  * a CUDA error, else DSA_OK.
+ * There is ONE status word per device, shared by every stream and host thread
+ * that uses the library on it: the first device error since the last read
+ * wins, whatever stream raised it.  Only `stream` is synchronised, so an error
+ * raised by a kernel still running on another stream may be reported by a
+ * later call, and this call clears errors of other streams too.  Callers
+ * that run several streams read the status after synchronising all of them.
  */
 int dsa_get_status(dsa_stream_t stream, int *device_status);
 

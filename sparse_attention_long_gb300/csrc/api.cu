@@ -4,6 +4,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "dsa_common.cuh"
 
 namespace dsa {
@@ -49,17 +51,48 @@ int launch_kl_bwd_tc(const Shape& s, const void* q, const void* kv, const void* 
                      DevCtx c, cudaStream_t st);
 
 // ------------------------------ status word --------------------------------
+// One status word per device (shared by every stream and host thread using
+// that device).  Its device address is cached per device together with the
+// CUDA context it was looked up in, and looked up again when the current
+// context differs (after cudaDeviceReset the module, and the word, are
+// reloaded at a new address).
 __device__ int g_status;
 static unsigned long long g_budget_ns = 2000000000ull;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CUcontext current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (CtxGetCurrentFn)p;
+  });
+  CUcontext ctx = nullptr;
+  if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+  return ctx;
+}
+
+static std::mutex g_status_mu;
+static CUcontext g_status_ctx[64];
 static int* g_status_ptr[64];
 
 static bool dev_ctx(DevCtx* c) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  if (!g_status_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  CUcontext ctx = current_context();  // null before the runtime's first call on this thread
+  if (!ctx || !g_status_ptr[dev] || g_status_ctx[dev] != ctx) {
+    void* p = nullptr;  // (the lookup makes the device's context current if none is)
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess || !p) return false;
+    ctx = current_context();
+    if (!ctx) return false;
     g_status_ptr[dev] = (int*)p;
+    g_status_ctx[dev] = ctx;
   }
   c->status = g_status_ptr[dev];
   c->budget = g_budget_ns;

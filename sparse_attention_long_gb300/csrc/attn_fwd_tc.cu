@@ -98,16 +98,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// 16-byte global -> shared copy that bypasses registers (L2 only)
-__device__ __forceinline__ void cp_async16_cg(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-// arrive on `bar` once every cp.async this thread issued before has landed
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 // Non-blocking phase test (mbarrier.test_wait never suspends the thread,
 // unlike try_wait), for the MMA issuer's loop over several conditions.
 __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {

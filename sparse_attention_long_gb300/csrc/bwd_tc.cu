@@ -26,16 +26,6 @@
 namespace dsa {
 namespace bwd {
 
-// 16-byte global -> shared copy that bypasses registers (L2 only)
-__device__ __forceinline__ void cp_async16_cg(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-// arrive on `bar` once every cp.async this thread issued before has landed
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 constexpr int kH = 128, kDQK = 576, kDV = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 

@@ -29,16 +29,6 @@
 namespace dsa {
 namespace kltc {
 
-// 16-byte global -> shared copy that bypasses registers (L2 only)
-__device__ __forceinline__ void cp_async16_cg(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-// arrive on `bar` once every cp.async this thread issued before has landed
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 constexpr int kHI = 64, kDI = 128, kTile = 128, kMaxK = 2048;
 constexpr int kThreads = 160;
 constexpr uint32_t kColS = 0, kColDK = 64, kColDQ = 192;   // TMEM columns

@@ -9,11 +9,14 @@
 //
 // The ring is a file-scope device array of kStaticRingBytes (32 MiB); every
 // GPU that loads this library keeps it until the process exits.  Its device
-// address is looked up once per device, on the first call made with that
-// device current (so make that first call before any stream capture).
+// address is looked up by the first call made with that device current (so
+// make that first call before any stream capture), and again only when the
+// device's CUDA context has changed since (e.g. after cudaDeviceReset).
 // Every call shares the one ring: calls that overlap on the GPU (other
 // streams, other host threads) race on it.  The ring needs no clearing: each
 // wave's indexer writes every score its top-k then reads.
+#include <mutex>
+
 #include "dsa_common.cuh"
 
 namespace dsa {
@@ -29,9 +32,16 @@ int ext_attn_fwd(const dsa_params* p, const Shape& s, const void* q, const void*
 int launch_topk(const Shape& s, const float* scores, long long ld, long long row_begin,
                 long long rows, int32_t* idx, DevCtx c, cudaStream_t st);
 
+CUcontext current_context();
+
 constexpr size_t kStaticRingBytes = 32ull << 20;
 static __device__ __align__(256) float g_static_ring[kStaticRingBytes / sizeof(float)];
-static float* g_static_ring_addr[64];  // device address of g_static_ring, per device
+// device address of g_static_ring per device, with the context it was looked
+// up in (looked up again when the current context differs, e.g. after
+// cudaDeviceReset reloaded the module)
+static std::mutex g_ring_mu;
+static CUcontext g_ring_ctx[64];
+static float* g_static_ring_addr[64];
 
 }  // namespace dsa
 
@@ -58,15 +68,23 @@ extern "C" int dsa_forward_static_ws(const dsa_params* p, const void* q_I, const
   if (W > total) W = total;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DSA_ERR_CUDA;
-  if (!g_static_ring_addr[dev]) {
-    float* ptr = nullptr;
-    if (cudaGetSymbolAddress((void**)&ptr, g_static_ring) != cudaSuccess || !ptr)
-      return DSA_ERR_CUDA;
-    g_static_ring_addr[dev] = ptr;
-  }
-  float* ring = g_static_ring_addr[dev];
   DevCtx c;
   if (!ext_dev_ctx(&c)) return DSA_ERR_CUDA;
+  float* ring = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_ring_mu);
+    CUcontext ctx = current_context();
+    if (!ctx || !g_static_ring_addr[dev] || g_ring_ctx[dev] != ctx) {
+      float* ptr = nullptr;
+      if (cudaGetSymbolAddress((void**)&ptr, g_static_ring) != cudaSuccess || !ptr)
+        return DSA_ERR_CUDA;
+      ctx = current_context();
+      if (!ctx) return DSA_ERR_CUDA;
+      g_static_ring_addr[dev] = ptr;
+      g_ring_ctx[dev] = ctx;
+    }
+    ring = g_static_ring_addr[dev];
+  }
   cudaStream_t st = (cudaStream_t)stream;
   for (long long r0 = 0; r0 < total; r0 += W) {
     const long long n = (total - r0) < W ? (total - r0) : W;
