@@ -109,11 +109,12 @@ def time_calls(fn, steps, warmup, stream):
     return a.elapsed_time(b) / steps
 
 
-def backward_stage(dsa, dev, steps, peak_tc):
+def backward_stage(dsa, dev, steps, peak_tc, workload="dsv32_S16384_train"):
     """The training-shape backward (S = 16384, top-2048, all rows): the forward,
     the attention backward (dq, dkv), the indexer KL-loss backward, each timed
-    alone, and dsa_backward (both in one call sharing the recompute of P)."""
-    wl = synth.WORKLOADS["dsv32_S16384_train"]
+    alone, and dsa_backward (both in one call sharing the recompute of P).
+    `workload` picks another shape (a smaller one for profiling)."""
+    wl = synth.WORKLOADS[workload]
     S, k, H = wl["S"], wl["topk"], wl["H"]
     x = synth.make_inputs(wl, device=dev, with_dout=True)
     p = dsa.make_params(B=1, S_q=S, S_k=S, H=H, d_qk=wl["d_qk"], d_v=wl["d_v"], H_I=wl["H_I"],
@@ -368,7 +369,8 @@ def main():
         print(json.dumps(topk_stage(dsa, dev, wl, args.steps, args.warmup, load_peaks())), flush=True)
         return
     if args.stage == "bwd":
-        bwd = backward_stage(dsa, dev, args.steps, load_peaks()["bf16_tflops_sustained"])
+        wname = args.workload if args.workload != "dsv32_S32768" else "dsv32_S16384_train"
+        bwd = backward_stage(dsa, dev, args.steps, load_peaks()["bf16_tflops_sustained"], wname)
         print(json.dumps(dict(stage="bwd", **bwd)), flush=True)
         return
 
