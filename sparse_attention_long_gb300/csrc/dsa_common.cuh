@@ -275,6 +275,33 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+// 16 / 8 consecutive columns (same lane mapping as tmem_ld32); the caller
+// ties the destinations to a following tcgen05.wait::ld (tmem_ld_also16/8)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : DSA_R8(0), DSA_R8(8)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : DSA_R8(0)
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_also16(uint32_t (&r)[16]) {
+  asm volatile("" : DSA_RW8(0), DSA_RW8(8) : : "memory");
+}
+__device__ __forceinline__ void tmem_ld_also8(uint32_t (&r)[8]) {
+  asm volatile("" : DSA_RW8(0) : : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      DSA_W8(0), DSA_W8(8)
+      : "memory");
+}
+
 __device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c),
                "f"(d)
