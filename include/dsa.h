@@ -150,6 +150,9 @@ int dsa_topk(const dsa_params *p, const float *scores, int64_t row_begin, int64_
  *       m = max_i scale*q.k_i,  l = sum_i exp(scale*q.k_i - m) over valid i
  *       ([HP-CP] DSA indexer-loss boundary carries softmax_max/softmax_sum).
  *       A row with no valid index gives out = 0, m = -inf, l = 0.
+ *   bf16 path: DeepSeek head shapes only (H 128, d_qk 576, d_v 512) with
+ *       topk <= 2048, else DSA_ERR_UNSUPPORTED; q, kv and out 16-byte aligned,
+ *       else DSA_ERR_INVALID_ARG.
  *   workspace: dsa_workspace_size(p, DSA_CALL_ATTN_FWD) bytes (may be NULL if 0).
  */
 int dsa_sparse_attn_fwd(const dsa_params *p, const void *q, const void *kv, const int32_t *idx,

@@ -204,10 +204,11 @@ static int indexer_rows(const dsa_params* p, const Shape& s, const void* q_I, co
   return launch_simt_indexer(s, bf16, q_I, k_I, w, row_begin, rows, scores, ld, fill ? 1 : 0, c, st);
 }
 
-static int attn_fwd_supported(const dsa_params* p, const Shape& s, const void* q, const void* kv) {
+static int attn_fwd_supported(const dsa_params* p, const Shape& s, const void* q, const void* kv,
+                              const void* out) {
   if (p->dtype == DSA_BF16) {
     if (!tc_attn_shape(p) || p->topk > 2048) return DSA_ERR_UNSUPPORTED;
-    if (!aligned16(q) || !aligned16(kv)) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kv) || !aligned16(out)) return DSA_ERR_INVALID_ARG;
     return DSA_OK;
   }
   return simt_smem_attn_fwd(s) > 200 * 1024 ? DSA_ERR_UNSUPPORTED : DSA_OK;
@@ -309,7 +310,7 @@ int dsa_sparse_attn_fwd(const dsa_params* p, const void* q, const void* kv, cons
   int rc = check_params(p, &s);
   if (rc) return rc;
   if (!q || !kv || !idx || !out || !softmax_max || !softmax_sum) return DSA_ERR_INVALID_ARG;
-  rc = attn_fwd_supported(p, s, q, kv);
+  rc = attn_fwd_supported(p, s, q, kv, out);
   if (rc) return rc;
   DevCtx c;
   if (!dev_ctx(&c)) return DSA_ERR_CUDA;
@@ -410,7 +411,7 @@ int dsa_forward(const dsa_params* p, const void* q_I, const void* k_I, const voi
   if (!q_I || !k_I || !w || !q || !kv || !idx_out || !out || !softmax_max || !softmax_sum)
     return DSA_ERR_INVALID_ARG;
   if (!workspace || !aligned16(workspace)) return DSA_ERR_WORKSPACE;
-  rc = attn_fwd_supported(p, s, q, kv);
+  rc = attn_fwd_supported(p, s, q, kv, out);
   if (rc) return rc;
   if (p->dtype == DSA_BF16 && (!aligned16(q_I) || !aligned16(k_I))) return DSA_ERR_INVALID_ARG;
   DevCtx c;
@@ -478,8 +479,9 @@ extern "C" int dsa_selftest_wait_timeout(uint64_t budget_ns, dsa_stream_t stream
 namespace dsa {
 int ext_check_params(const dsa_params* p, Shape* s) { return check_params(p, s); }
 bool ext_dev_ctx(DevCtx* c) { return dev_ctx(c); }
-int ext_attn_fwd_supported(const dsa_params* p, const Shape& s, const void* q, const void* kv) {
-  return attn_fwd_supported(p, s, q, kv);
+int ext_attn_fwd_supported(const dsa_params* p, const Shape& s, const void* q, const void* kv,
+                           const void* out) {
+  return attn_fwd_supported(p, s, q, kv, out);
 }
 int ext_indexer_rows(const dsa_params* p, const Shape& s, const void* q_I, const void* k_I,
                      const void* w, long long row_begin, long long rows, float* scores,

@@ -195,11 +195,56 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) 
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// query columns of one head for one lane half (see the softmax role)
+__device__ __forceinline__ const __nv_bfloat16* q_head(const __nv_bfloat16* qb, long long row,
+                                                      uint32_t crank, int hl) {
+  return qb + (row * kH + kHC * crank + hl) * (long long)kDQK;
+}
+__device__ __forceinline__ void q_fetch_value(const __nv_bfloat16* qh, int ch, int half, uint32_t (&w0)[32],
+                                              uint32_t (&w1)[32]) {
+  const uint4* src = reinterpret_cast<const uint4*>(qh + 256 * ch + 128 * half);
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    const uint4 a = __ldg(src + t), b = __ldg(src + 8 + t);
+    w0[4 * t] = a.x;
+    w0[4 * t + 1] = a.y;
+    w0[4 * t + 2] = a.z;
+    w0[4 * t + 3] = a.w;
+    w1[4 * t] = b.x;
+    w1[4 * t + 1] = b.y;
+    w1[4 * t + 2] = b.z;
+    w1[4 * t + 3] = b.w;
+  }
+}
+// ... and into TMEM (lane_tmem = TMEM base with this warp's lane quadrant);
+// the rope columns (column half 0 only) are loaded here
+__device__ __forceinline__ void q_store(uint32_t lane_tmem, const __nv_bfloat16* qh, int ch, int half,
+                                        const uint32_t (&w0)[32], const uint32_t (&w1)[32]) {
+  tmem_st32(lane_tmem + kColQ + 64 * ch, w0);
+  tmem_st32(lane_tmem + kColQ + 64 * ch + 32, w1);
+  if (ch == 0) {
+    const uint4* rsrc = reinterpret_cast<const uint4*>(qh + kDV + 32 * half);
+    uint32_t w2[16];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint4 a = __ldg(rsrc + t);
+      w2[4 * t] = a.x;
+      w2[4 * t + 1] = a.y;
+      w2[4 * t + 2] = a.z;
+      w2[4 * t + 3] = a.w;
+    }
+    tmem_st16(lane_tmem + kColQ + 128, w2);
+  }
+  tmem_st_wait();
+  tc_fence_before();
+  __syncwarp();
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const void* __restrict__ qg, const void* __restrict__ kvg, Shape s,
                        const int32_t* __restrict__ idx, __nv_bfloat16* __restrict__ out,
                        float* __restrict__ mx, float* __restrict__ sm_out, long long nrows,
-                       DevCtx c) {
+                       DevCtx c, const __grid_constant__ CUtensorMap tmo) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -484,56 +529,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     };
-    // query columns of head hl for lane half `half` into TMEM: run ch of E_half
-    // (128 contiguous columns) -> columns kColQ + 64ch .. +64, and (ch 0) the
-    // rope columns R_half -> kColQ + 128 .. +16; then arrive on q_tm[bi]
-    auto load_q = [&](long long row, int bi) {
-      const __nv_bfloat16* qh = qb + (row * kH + kHC * crank + hl) * (long long)kDQK;
-      const uint4* src = reinterpret_cast<const uint4*>(qh + 256 * ch + 128 * half);
-      const uint4* rsrc = reinterpret_cast<const uint4*>(qh + kDV + 32 * half);
-      uint32_t w0[32], w1[32], w2[16];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const uint4 a = __ldg(src + t), b2 = __ldg(src + 8 + t);
-        w0[4 * t] = a.x;
-        w0[4 * t + 1] = a.y;
-        w0[4 * t + 2] = a.z;
-        w0[4 * t + 3] = a.w;
-        w1[4 * t] = b2.x;
-        w1[4 * t + 1] = b2.y;
-        w1[4 * t + 2] = b2.z;
-        w1[4 * t + 3] = b2.w;
-      }
-      if (ch == 0) {
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const uint4 a = __ldg(rsrc + t);
-          w2[4 * t] = a.x;
-          w2[4 * t + 1] = a.y;
-          w2[4 * t + 2] = a.z;
-          w2[4 * t + 3] = a.w;
-        }
-      }
-      tmem_st32(tmem + lane_off + kColQ + 64 * ch, w0);
-      tmem_st32(tmem + lane_off + kColQ + 64 * ch + 32, w1);
-      if (ch == 0) tmem_st16(tmem + lane_off + kColQ + 128, w2);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      signal(&sm.q_tm[bi]);
-    };
-
+    // Query columns of head hl for lane half `half`: run ch of E_half (128
+    // contiguous columns) -> TMEM columns kColQ + 64ch .. +64, and (ch 0) the
+    // rope columns R_half -> kColQ + 128 .. +16 (q_fetch_value: the value
+    // columns into registers; q_store: into TMEM with the rope columns, then
+    // the signal on q_tm[bi]).
     // The 8 softmax warps synchronise with each other through named barriers
     // 1 (bar.sync, 256 threads) and 2 (the per-token vote): every warp
     // executes the same sequence of barriers whatever happens (after a failed
     // wait it keeps going through the token without work, and the vote at the
     // next token makes all of them stop), so they cannot deadlock.
     bool ok = true;
-    if (ntok > 0) load_q(nrows - 1 - pair, 0);
+    if (ntok > 0) {
+      uint32_t w0[32], w1[32];
+      const __nv_bfloat16* qh = q_head(qb, nrows - 1 - pair, crank, hl);
+      q_fetch_value(qh, ch, half, w0, w1);
+      q_store(tmem + lane_off, qh, ch, half, w0, w1);
+      signal(&sm.q_tm[0]);
+    }
+    // the epilogue stages O through the P buffers; one thread stores them
+    // with TMA and waits for those reads before the buffers are reused
+    const bool o_storer = warp == kWarpSoft0 && lane == 0;
     int G = 0;  // blocks so far (all tokens)
     for (int i = 0; i < ntok; ++i) {
       const int bi = i & 1;
       const long long row = nrows - 1 - (pair + (long long)i * npairs);
+      if (o_storer) bulk_wait_read_all();
       if (ok) ok = mbar_wait_warp(smem_u32(&sm.sc_full[bi]), (i >> 1) & 1, c, abort_flag);
       if (named_bar_or(2, kSoftWarps * 32, !ok)) break;
       const int nblk = sm.nblk[bi];
@@ -707,8 +728,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // this token's masks are no longer read
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.sc_empty[bi]));
-      // the next token's query (this token's last logits have been read)
-      if (ok && i + 1 < ntok) load_q(row - npairs, (i + 1) & 1);
+      // the next token's query into TMEM (this token's last logits have been
+      // read, so its columns are free) before the epilogue, so that the
+      // next token's first logits run during the epilogue (holding the
+      // query in registers across the epilogue spills)
+      const bool next_q = ok && i + 1 < ntok;
+      if (next_q) {
+        uint32_t w0[32], w1[32];
+        const __nv_bfloat16* qh = q_head(qb, row - npairs, crank, hl);
+        q_fetch_value(qh, ch, half, w0, w1);
+        q_store(tmem + lane_off, qh, ch, half, w0, w1);
+        signal(&sm.q_tm[(i + 1) & 1]);
+      }
       // ------------------------------- epilogue -------------------------------
       bool have = ok;
       if (have) have = mbar_wait_warp(smem_u32(&sm.mma_done[bi]), (i >> 1) & 1, c, abort_flag);
@@ -722,30 +753,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const float lsum = (sm.red[quad][lane] + sm.red[quad + 4][lane]) +
                          (sm.red[quad ^ 2][lane] + sm.red[(quad ^ 2) + 4][lane]);
       const float inv = (have && lsum > 0.f) ? 1.f / lsum : 0.f;
-      __nv_bfloat16* orow = out + (row * kH + kHC * crank + hl) * (long long)kDV;
       const bool all_have = __all_sync(0xffffffffu, have);
+      // O (bf16) out through shared memory, in two rounds m = 0, 1: value
+      // columns [256m, 256m+256) of the CTA's 64 heads fill both P buffers
+      // (32 KB, free: every PV of this token has completed) as four 64-column
+      // tiles [64 heads][128 B] with the 128-byte swizzle, stored by TMA.
+      // This thread writes row hl of tile 2*half + ch (value columns 256m +
+      // 128half + 64ch .. +64).
+      uint8_t* const ostage = &sm.p[0][0];
+      uint8_t* const trow = ostage + (2 * half + ch) * (kHC * 128) + hl * 128;
 #pragma unroll 1
       for (int m = 0; m < 2; ++m) {
-        uint32_t o0[32], o1[32];
-        if (all_have) {
-          tmem_ld32(tmem + lane_off + kColO + 128 * m + 64 * ch, o0);
-          tmem_ld32(tmem + lane_off + kColO + 128 * m + 64 * ch + 32, o1);
-          tmem_ld_wait(o0);
-          tmem_ld_also(o1);
-        } else {
-#pragma unroll
-          for (int t = 0; t < 32; ++t) o0[t] = o1[t] = 0u;
+        if (m == 1) {  // round 0's tiles read out of shared memory before they are overwritten
+          if (o_storer) bulk_wait_read_all();
+          named_bar_sync(1, kSoftWarps * 32);
         }
-        uint4 pk4[8];
-        uint32_t* pw = reinterpret_cast<uint32_t*>(pk4);
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          pw[t] = pack_bf16x2(__uint_as_float(o0[2 * t]) * inv, __uint_as_float(o0[2 * t + 1]) * inv);
-          pw[16 + t] = pack_bf16x2(__uint_as_float(o1[2 * t]) * inv, __uint_as_float(o1[2 * t + 1]) * inv);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t o[16];
+          if (all_have) {
+            tmem_ld16(tmem + lane_off + kColO + 128 * m + 64 * ch + 16 * q4, o);
+            tmem_ld_wait16(o);
+          } else {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) o[t] = 0u;
+          }
+          uint32_t pw[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            pw[t] = pack_bf16x2(__uint_as_float(o[2 * t]) * inv, __uint_as_float(o[2 * t + 1]) * inv);
+          *reinterpret_cast<uint4*>(trow + (((2 * q4) ^ (hl & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+          *reinterpret_cast<uint4*>(trow + (((2 * q4 + 1) ^ (hl & 7)) << 4)) =
+              make_uint4(pw[4], pw[5], pw[6], pw[7]);
         }
-        uint4* dst = reinterpret_cast<uint4*>(orow + 256 * m + 128 * half + 64 * ch);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) dst[t] = pk4[t];
+        fence_proxy_async_smem();
+        named_bar_sync(1, kSoftWarps * 32);
+        if (o_storer) {
+          const int y = (int)(row * kH + kHC * crank);
+#pragma unroll 1
+          for (int tt = 0; tt < 4; ++tt) tma_store_2d(&tmo, smem_u32(ostage + tt * (kHC * 128)), 256 * m + 64 * tt, y);
+          bulk_commit_group();
+        }
       }
       tc_fence_before();  // O is overwritten by the next token's first PV
       if (half == 0 && ch == 0) {
@@ -755,6 +803,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         sm_out[hrow] = any ? lsum * ex2(m_run - m_true) : 0.f;
       }
     }
+    if (o_storer) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -766,6 +815,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 }  // namespace attn
+
+bool make_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
+                       uint32_t box_cols, uint32_t box_rows, int swizzle_bytes);
 
 int attn_fwd_tc_max_topk() { return attn::kMaxTopk; }
 
@@ -799,10 +851,14 @@ int launch_attn_fwd_tc(const Shape& s, const void* q, const void* kv, const int3
     pairs = clusters;
     if (dev < 64) pairs_by_device[dev] = pairs;
   }
+  if (nrows * kH > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
   const long long grid_pairs = nrows < pairs ? nrows : pairs;
+  // O stores: [rows * 128 heads][512] bf16 in 64 x 64 tiles, 128-byte swizzle
+  CUtensorMap tmo;
+  if (!make_tmap_2d_bf16(&tmo, out, (uint64_t)nrows * kH, kDV, 64, kHC, 128)) return DSA_ERR_CUDA;
   attn_fwd_tc_kernel<<<(unsigned)(2 * grid_pairs), kThreads, smem, st>>>(q, kv, s, idx,
                                                                           (__nv_bfloat16*)out, mx, sm,
-                                                                          nrows, c);
+                                                                          nrows, c, tmo);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

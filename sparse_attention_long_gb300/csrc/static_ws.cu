@@ -23,7 +23,8 @@ namespace dsa {
 
 int ext_check_params(const dsa_params* p, Shape* s);
 bool ext_dev_ctx(DevCtx* c);
-int ext_attn_fwd_supported(const dsa_params* p, const Shape& s, const void* q, const void* kv);
+int ext_attn_fwd_supported(const dsa_params* p, const Shape& s, const void* q, const void* kv,
+                           const void* out);
 int ext_indexer_rows(const dsa_params* p, const Shape& s, const void* q_I, const void* k_I,
                      const void* w, long long row_begin, long long rows, float* scores,
                      long long ld, DevCtx c, cudaStream_t st);
@@ -56,7 +57,7 @@ extern "C" int dsa_forward_static_ws(const dsa_params* p, const void* q_I, const
   if (rc) return rc;
   if (!q_I || !k_I || !w || !q || !kv || !idx_out || !out || !softmax_max || !softmax_sum)
     return DSA_ERR_INVALID_ARG;
-  rc = ext_attn_fwd_supported(p, s, q, kv);
+  rc = ext_attn_fwd_supported(p, s, q, kv, out);
   if (rc) return rc;
   if (p->dtype == DSA_BF16 &&
       ((((uintptr_t)q_I) & 15u) != 0 || (((uintptr_t)k_I) & 15u) != 0))

@@ -69,6 +69,13 @@ def test_host_validation_without_gpu():
                          scale=0.5, dtype="bf16")
     assert dsa.lib.dsa_sparse_attn_fwd(ctypes.byref(bf), 16, 16, 16, 16, 16, 16, None, None) == \
         dsa.DSA_ERR_UNSUPPORTED
+    # the bf16 path stores O with TMA: q, kv and out must be 16-byte aligned
+    ds = dsa.make_params(B=1, S_q=8, S_k=8, H=128, d_qk=576, d_v=512, H_I=64, d_I=128, topk=4,
+                         scale=0.5, dtype="bf16")
+    assert dsa.lib.dsa_sparse_attn_fwd(ctypes.byref(ds), 16, 16, 16, 24, 16, 16, None, None) == \
+        dsa.DSA_ERR_INVALID_ARG
+    assert dsa.lib.dsa_sparse_attn_fwd(ctypes.byref(ds), 16, 8, 16, 16, 16, 16, None, None) == \
+        dsa.DSA_ERR_INVALID_ARG
 
 
 def test_backward_workspace_sizes():
