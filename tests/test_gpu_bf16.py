@@ -272,3 +272,53 @@ def test_cp4_head_tail_shard_at_32k():
     assert ok, (ma, mr)
     assert np.abs(np64(sh["m"])[0, local] - m[0]).max() < 1e-4
     assert (np.abs(np64(sh["l"])[0, local] - l[0]) / l[0]).max() < 1e-4
+
+
+def test_attention_edge_rows_two_batches():
+    # Index rows that stress the persistent CTA-pair pipeline: rows with no
+    # valid slot between full rows (no blocks at all), a single valid slot at
+    # the far end (every earlier block empty), a single slot at the start,
+    # -1 holes, repeated indices, and out-of-order rows; two batches (kv of
+    # batch b only), k not a multiple of the 112-slot block.
+    dsa = lib()
+    wl = dict(synth.v32(160, "edge"), B=2, topk=250)
+    x = synth.make_inputs(wl)
+    B, S, k = 2, wl["S"], wl["topk"]
+    rng = np.random.default_rng(7)
+    idx = np.full((B, S, k), -1, dtype=np.int32)
+    for b in range(B):
+        for t in range(S):
+            kind = (t + b) % 7
+            if kind == 0:
+                continue                                   # nothing valid
+            if kind == 1:
+                idx[b, t, k - 1] = rng.integers(0, S)       # only the last slot
+            elif kind == 2:
+                idx[b, t, 0] = rng.integers(0, S)           # only the first slot
+            elif kind == 3:
+                idx[b, t, :] = rng.integers(0, S, size=k)   # full, with repeats
+            elif kind == 4:
+                row = rng.integers(0, S, size=k)
+                row[::2] = -1                               # holes
+                idx[b, t, :] = row
+            elif kind == 5:
+                n = min(S, k)
+                idx[b, t, :n] = rng.permutation(S)[:n]      # distinct, shuffled
+            else:
+                idx[b, t, 112:224] = rng.integers(0, S, size=112)  # only the middle block
+    O, m, l = oracle.sparse_attn_fwd(x["q"], x["kv"], idx, wl["scale"], 512)
+    p = params(dsa, wl)
+    o = empty_outputs(wl, S, torch.bfloat16)
+    dsa.sparse_attn_fwd(p, x["q"].to(DEV), x["kv"].to(DEV), torch.as_tensor(idx, device=DEV),
+                        o["out"], o["m"], o["l"])
+    torch.cuda.synchronize()
+    assert dsa.get_status() == 0
+    got = np64(o["out"])
+    empty = np.all(idx < 0, axis=2)
+    assert np.all(got[empty] == 0.0)
+    assert np.all(np.isneginf(np64(o["m"])[empty])) and np.all(np64(o["l"])[empty] == 0.0)
+    ok, ma, mr = bf16_close(got[~empty], O[~empty])
+    assert ok, (ma, mr)
+    mg, lg = np64(o["m"])[~empty], np64(o["l"])[~empty]
+    assert np.abs(mg - m[~empty]).max() < 1e-4
+    assert (np.abs(lg - l[~empty]) / l[~empty]).max() < 1e-4
