@@ -109,6 +109,33 @@ def time_calls(fn, steps, warmup, stream):
     return a.elapsed_time(b) / steps
 
 
+def fp8_indexer_stage(dsa, dev, wl, x, waves, steps, peak_tc):
+    """The FP8 (E4M3) indexer on the same rows as the step, outside the timed
+    step: the quantization of q_I and k_I, then every wave of scores.  Its
+    tensor peak is the bf16 peak x 2 (the nominal FP8 / BF16 ratio)."""
+    S = wl["S"]
+    p = dsa.make_params(B=1, S_q=S, S_k=S, H=wl["H"], d_qk=wl["d_qk"], d_v=wl["d_v"], H_I=wl["H_I"],
+                        d_I=wl["d_I"], topk=wl["topk"], scale=wl["scale"], dtype="bf16", flags=1)
+    q8 = torch.empty(1, S, wl["H_I"], wl["d_I"], dtype=torch.uint8, device=dev)
+    sq = torch.empty(1, S, wl["H_I"], device=dev)
+    k8 = torch.empty(1, S, wl["d_I"], dtype=torch.uint8, device=dev)
+    sk = torch.empty(1, S, device=dev)
+    ring = torch.empty(max(n for _, n in waves), S, device=dev)
+    st = torch.cuda.current_stream(dev)
+    t_q = time_calls(lambda: dsa.indexer_quantize_fp8(p, x["q_I"], x["k_I"], q8, sq, k8, sk), steps, 2, st)
+
+    def scores():
+        for r0, n in waves:
+            dsa.indexer_scores_fp8(p, q8, sq, k8, sk, x["w"], r0, n, ring)
+    t_s = time_calls(scores, steps, 2, st)
+    assert dsa.get_status() == 0
+    f_idx, _, _ = algorithmic(wl, np.arange(S))
+    tflops = f_idx / (t_s * 1e-3) / 1e12
+    return {"quantize_ms": t_q, "scores_ms": t_s, "tflops": tflops, "peak_fp8": 2 * peak_tc,
+            "frac": tflops / (2 * peak_tc),
+            "note": "E4M3 q_I, k_I with one fp32 scale per 128-vector; outside the timed step"}
+
+
 def backward_stage(dsa, dev, steps, peak_tc, workload="dsv32_S16384_train"):
     """The training-shape backward (S = 16384, top-2048, all rows): the forward,
     the attention backward (dq, dkv), the indexer KL-loss backward, each timed
@@ -554,6 +581,9 @@ def main():
                "equals_whole_call": same}
         assert dsa.get_status() == 0
 
+    fp8i = None
+    if rank == 0:
+        fp8i = fp8_indexer_stage(dsa, dev, wl, x, waves, max(2, min(K, 5)), peak_tc)
     bwd = None
     if not args.no_bwd and rank == 0:
         del x, out, ring, idx, m, l, flush
@@ -601,6 +631,7 @@ def main():
         "e2e": e2e,
         "cpu_baseline": cpu,
         "backward": bwd,
+        "fp8_indexer": fp8i,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -69,9 +69,11 @@ enum { DSA_BF16 = 0, DSA_FP32 = 1 };
  * "ulysses" is an error there and is DSA_ERR_UNSUPPORTED here. */
 enum { DSA_CP_COLOSSAL = 0, DSA_CP_ULYSSES = 1 };
 
-/* dsa_params.flags: dsa_indexer_scores writes only the causal entries
- * s <= pos(t) and leaves the rest of each score row untouched. */
-enum { DSA_FLAG_CAUSAL_ONLY = 1 };
+/* dsa_params.flags: DSA_FLAG_CAUSAL_ONLY: dsa_indexer_scores(_fp8) writes
+ * only the causal entries s <= pos(t) and leaves the rest of each score row
+ * untouched.  DSA_FLAG_FP8_INDEXER: dsa_forward scores with the FP8 (E4M3)
+ * indexer of dsa_indexer_scores_fp8 (DeepSeek indexer shapes, bf16). */
+enum { DSA_FLAG_CAUSAL_ONLY = 1, DSA_FLAG_FP8_INDEXER = 2 };
 
 /* workspace queries (dsa_workspace_size `which`) */
 enum {
@@ -121,6 +123,34 @@ size_t dsa_workspace_size(const dsa_params *p, int which);
  */
 int dsa_indexer_scores(const dsa_params *p, const void *q_I, const void *k_I, const void *w,
                        int64_t row_begin, int64_t rows, float *scores, dsa_stream_t stream);
+
+/*
+ * FP8 (E4M3) Lightning Indexer.  The pages give no DSA FP8 recipe (they name
+ * FP8 / MxFP8 for the MoE layers only, [DSA-32K] "Why TorchTitan"); this is
+ * one reading of it: q_I and k_I are quantized per 128-element vector to
+ * E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, largest finite
+ * value 448, no infinities) with scale = absmax / 448 in fp32 (1 for an
+ * all-zero vector), each element x / scale rounded to nearest even and
+ * clamped to +-448; the score is the Lightning Indexer formula on the
+ * dequantized vectors:
+ *   I[t, s] = sum_j w[t, j] * ReLU(sq[t, j] * sk[s] * (q8[t, j, :] . k8[s, :])).
+ * DeepSeek indexer shapes only (H_I 64, d_I 128) and dtype DSA_BF16, else
+ * DSA_ERR_UNSUPPORTED.
+ *
+ * dsa_indexer_quantize_fp8: q_I [B, S_q, H_I, 128] and k_I [B, S_k, 128]
+ *   bf16 (16-byte aligned) -> q8 [B, S_q, H_I, 128] and k8 [B, S_k, 128] E4M3
+ *   codes (16-byte aligned, caller-owned), q_scale [B, S_q, H_I] and
+ *   k_scale [B, S_k] fp32.
+ * dsa_indexer_scores_fp8: the scores of flattened rows [row_begin,
+ *   row_begin + rows) from those buffers, w [B, S_q, H_I] bf16; output and
+ *   flags as dsa_indexer_scores.  Dot products of E4M3 values are exact
+ *   products accumulated in fp32.
+ */
+int dsa_indexer_quantize_fp8(const dsa_params *p, const void *q_I, const void *k_I, uint8_t *q8,
+                             float *q_scale, uint8_t *k8, float *k_scale, dsa_stream_t stream);
+int dsa_indexer_scores_fp8(const dsa_params *p, const uint8_t *q8, const float *q_scale,
+                           const uint8_t *k8, const float *k_scale, const void *w, int64_t row_begin,
+                           int64_t rows, float *scores, dsa_stream_t stream);
 
 /*
  * Per-query top-k.  [DSA-32K] "Top-k positions of each token" select the kv
@@ -231,6 +261,8 @@ int dsa_backward(const dsa_params *p, const void *q, const void *kv, const int32
  * Whole forward: indexer scores -> top-k -> sparse attention, the S x S score
  * matrix streamed through a workspace ring of wave_rows x S_k fp32 (never
  * materialised whole).  Outputs as in the calls above; idx_out [B, S_q, topk].
+ * With DSA_FLAG_FP8_INDEXER the scores come from the FP8 indexer (q_I and
+ * k_I quantized once per call into the workspace after the ring).
  *   workspace: dsa_workspace_size(p, DSA_CALL_FORWARD) bytes.
  */
 int dsa_forward(const dsa_params *p, const void *q_I, const void *k_I, const void *w,
@@ -250,7 +282,8 @@ int dsa_forward(const dsa_params *p, const void *q_I, const void *k_I, const voi
  * only if the device's CUDA context changed since.  All calls share the ring:
  * calls that overlap on the GPU race on it.
  * Returns DSA_ERR_UNSUPPORTED when S_k > 2,097,152 (4 score rows would not
- * fit the ring); never allocates or frees device memory.
+ * fit the ring) or with DSA_FLAG_FP8_INDEXER (bf16 indexer only); never
+ * allocates or frees device memory.
  */
 int dsa_forward_static_ws(const dsa_params *p, const void *q_I, const void *k_I, const void *w,
                           const void *q, const void *kv, int32_t *idx_out, void *out,

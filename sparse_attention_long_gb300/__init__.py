@@ -55,6 +55,8 @@ _sigs = {
     "dsa_version": ([], ctypes.c_int),
     "dsa_workspace_size": ([_P, ctypes.c_int], ctypes.c_size_t),
     "dsa_indexer_scores": ([_P, _vp, _vp, _vp, _i64, _i64, _vp, _vp], ctypes.c_int),
+    "dsa_indexer_quantize_fp8": ([_P] + [_vp] * 7, ctypes.c_int),
+    "dsa_indexer_scores_fp8": ([_P, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp], ctypes.c_int),
     "dsa_topk": ([_P, _vp, _i64, _i64, _vp, _vp], ctypes.c_int),
     "dsa_sparse_attn_fwd": ([_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
     "dsa_sparse_attn_bwd": ([_P] + [_vp] * 11, ctypes.c_int),
@@ -127,6 +129,18 @@ def workspace_size(p: dsa_params, which: int) -> int:
 def indexer_scores(p, q_I, k_I, w, row_begin, rows, scores, stream=None):
     _chk(lib.dsa_indexer_scores(ctypes.byref(p), _ptr(q_I), _ptr(k_I), _ptr(w), row_begin, rows,
                                 _ptr(scores), _stream(stream)), "dsa_indexer_scores")
+
+
+def indexer_quantize_fp8(p, q_I, k_I, q8, q_scale, k8, k_scale, stream=None):
+    _chk(lib.dsa_indexer_quantize_fp8(ctypes.byref(p), _ptr(q_I), _ptr(k_I), _ptr(q8), _ptr(q_scale),
+                                      _ptr(k8), _ptr(k_scale), _stream(stream)),
+         "dsa_indexer_quantize_fp8")
+
+
+def indexer_scores_fp8(p, q8, q_scale, k8, k_scale, w, row_begin, rows, scores, stream=None):
+    _chk(lib.dsa_indexer_scores_fp8(ctypes.byref(p), _ptr(q8), _ptr(q_scale), _ptr(k8), _ptr(k_scale),
+                                    _ptr(w), row_begin, rows, _ptr(scores), _stream(stream)),
+         "dsa_indexer_scores_fp8")
 
 
 def topk(p, scores, row_begin, rows, idx, stream=None):

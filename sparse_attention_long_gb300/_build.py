@@ -13,7 +13,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdsa_gb300.so")
 SOURCES = ["api.cu", "topk.cu", "simt.cu", "indexer_tc.cu", "attn_fwd_tc.cu", "static_ws.cu",
-           "bwd_tc.cu", "kl_tc.cu"]
+           "bwd_tc.cu", "kl_tc.cu", "indexer_fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include"), "-I", CSRC]

@@ -29,6 +29,10 @@ int launch_simt_kl_bwd(const Shape& s, bool bf16, const void* q, const void* kv,
 size_t simt_smem_attn_fwd(const Shape& s);
 size_t simt_smem_attn_bwd(const Shape& s);
 size_t simt_smem_kl(const Shape& s);
+int launch_quant_e4m3(const void* x, long long nrows, uint8_t* q, float* scale, cudaStream_t st);
+int launch_indexer_f8(const Shape& s, const uint8_t* q8, const float* q_scale, const uint8_t* k8,
+                      const float* k_scale, const void* w, long long row_begin, long long rows,
+                      float* scores, long long ld, DevCtx c, cudaStream_t st);
 int launch_indexer_tc(const Shape& s, const void* q_I, const void* k_I, const void* w,
                       long long row_begin, long long rows, float* scores, long long ld, DevCtx c,
                       cudaStream_t st);
@@ -134,6 +138,20 @@ bool make_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D uint8 tensor map [rows, cols] with a (box_cols x box_rows) box, 128-byte swizzle
+bool make_tmap_2d_u8(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                     uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // fp32 rows of `ld` floats viewed as [rows][lines][32]: line l of row r holds
 // columns [32l, 32l + 32); boxes of box_lines lines with the 128-byte swizzle
 bool make_tmap_f32_lines(CUtensorMap* tm, const float* base, uint64_t rows, uint64_t ld,
@@ -187,6 +205,24 @@ static int check_params(const dsa_params* p, Shape* s) {
   s->q_row_offset = p->q_row_offset;
   s->q_row_index = p->q_row_index;
   return DSA_OK;
+}
+
+// FP8 indexer operands in the forward's workspace, after the score ring:
+// q8 [B*S_q*H_I][128] | k8 [B*S_k][128] | q_scale [B*S_q*H_I] | k_scale [B*S_k],
+// each part 256-byte aligned
+struct Fp8Buffers {
+  size_t q8, k8, sq, sk, total;
+};
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+static Fp8Buffers fp8_buffers(const dsa_params* p) {
+  Fp8Buffers b;
+  const size_t nq = (size_t)(p->B * p->S_q * p->H_I), nk = (size_t)(p->B * p->S_k);
+  b.q8 = 0;
+  b.k8 = align256(nq * 128);
+  b.sq = b.k8 + align256(nk * 128);
+  b.sk = b.sq + align256(nq * 4);
+  b.total = b.sk + align256(nk * 4);
+  return b;
 }
 
 static int indexer_rows(const dsa_params* p, const Shape& s, const void* q_I, const void* k_I,
@@ -259,7 +295,11 @@ int dsa_version(void) { return 100; }
 size_t dsa_workspace_size(const dsa_params* p, int which) {
   Shape s;
   if (check_params(p, &s) != DSA_OK) return 0;
-  if (which == DSA_CALL_FORWARD) return (size_t)wave_rows(p) * (size_t)p->S_k * sizeof(float);
+  if (which == DSA_CALL_FORWARD) {
+    size_t bytes = (size_t)wave_rows(p) * (size_t)p->S_k * sizeof(float);
+    if (p->flags & DSA_FLAG_FP8_INDEXER) bytes = align256(bytes) + fp8_buffers(p).total;
+    return bytes;
+  }
   if (which == DSA_CALL_ATTN_BWD && tc_bwd_shape(p)) return bwd_tc_workspace(s);
   if (which == DSA_CALL_KL_BWD && tc_bwd_shape(p) && tc_indexer_shape(p)) return kl_tc_workspace(s);
   if (which == DSA_CALL_BACKWARD) {
@@ -288,6 +328,40 @@ int dsa_indexer_scores(const dsa_params* p, const void* q_I, const void* k_I, co
   const bool fill = (p->flags & DSA_FLAG_CAUSAL_ONLY) == 0;
   return indexer_rows(p, s, q_I, k_I, w, row_begin, rows, scores, p->S_k, fill, c,
                       (cudaStream_t)stream);
+}
+
+int dsa_indexer_quantize_fp8(const dsa_params* p, const void* q_I, const void* k_I, uint8_t* q8,
+                             float* q_scale, uint8_t* k8, float* k_scale, dsa_stream_t stream) {
+  Shape s;
+  int rc = check_params(p, &s);
+  if (rc) return rc;
+  if (p->dtype != DSA_BF16 || !tc_indexer_shape(p)) return DSA_ERR_UNSUPPORTED;
+  if (!q_I || !k_I || !q8 || !q_scale || !k8 || !k_scale) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_I) || !aligned16(k_I) || !aligned16(q8) || !aligned16(k8)) return DSA_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  rc = launch_quant_e4m3(q_I, p->B * p->S_q * p->H_I, q8, q_scale, st);
+  if (rc) return rc;
+  return launch_quant_e4m3(k_I, p->B * p->S_k, k8, k_scale, st);
+}
+
+int dsa_indexer_scores_fp8(const dsa_params* p, const uint8_t* q8, const float* q_scale,
+                           const uint8_t* k8, const float* k_scale, const void* w, int64_t row_begin,
+                           int64_t rows, float* scores, dsa_stream_t stream) {
+  Shape s;
+  int rc = check_params(p, &s);
+  if (rc) return rc;
+  if (p->dtype != DSA_BF16 || !tc_indexer_shape(p)) return DSA_ERR_UNSUPPORTED;
+  if (!q8 || !q_scale || !k8 || !k_scale || !w || !scores) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(k8)) return DSA_ERR_INVALID_ARG;
+  if (row_begin < 0 || rows < 1 || row_begin + rows > p->B * p->S_q) return DSA_ERR_INVALID_ARG;
+  DevCtx c;
+  if (!dev_ctx(&c)) return DSA_ERR_CUDA;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((p->flags & DSA_FLAG_CAUSAL_ONLY) == 0) {  // the kernel writes causal keys only: -inf elsewhere
+    rc = launch_simt_indexer(s, true, q8, q8, w, row_begin, rows, scores, p->S_k, 2, c, st);
+    if (rc) return rc;
+  }
+  return launch_indexer_f8(s, q8, q_scale, k8, k_scale, w, row_begin, rows, scores, p->S_k, c, st);
 }
 
 int dsa_topk(const dsa_params* p, const float* scores, int64_t row_begin, int64_t rows,
@@ -419,9 +493,26 @@ int dsa_forward(const dsa_params* p, const void* q_I, const void* k_I, const voi
   cudaStream_t st = (cudaStream_t)stream;
   const long long total = p->B * p->S_q, W = wave_rows(p);
   float* ring = (float*)workspace;
+  const bool fp8 = (p->flags & DSA_FLAG_FP8_INDEXER) != 0;
+  uint8_t *q8 = nullptr, *k8 = nullptr;
+  float *sq = nullptr, *sk = nullptr;
+  if (fp8) {
+    if (p->dtype != DSA_BF16 || !tc_indexer_shape(p)) return DSA_ERR_UNSUPPORTED;
+    const Fp8Buffers fb = fp8_buffers(p);
+    uint8_t* base = (uint8_t*)workspace + align256((size_t)W * (size_t)p->S_k * sizeof(float));
+    q8 = base + fb.q8;
+    k8 = base + fb.k8;
+    sq = (float*)(base + fb.sq);
+    sk = (float*)(base + fb.sk);
+    rc = launch_quant_e4m3(q_I, total * p->H_I, q8, sq, st);
+    if (rc) return rc;
+    rc = launch_quant_e4m3(k_I, p->B * p->S_k, k8, sk, st);
+    if (rc) return rc;
+  }
   for (long long r0 = 0; r0 < total; r0 += W) {
     const long long n = (total - r0) < W ? (total - r0) : W;
-    rc = indexer_rows(p, s, q_I, k_I, w, r0, n, ring, p->S_k, false, c, st);
+    rc = fp8 ? launch_indexer_f8(s, q8, sq, k8, sk, w, r0, n, ring, p->S_k, c, st)
+             : indexer_rows(p, s, q_I, k_I, w, r0, n, ring, p->S_k, false, c, st);
     if (rc) return rc;
     rc = launch_topk(s, ring, p->S_k, r0, n, idx_out + r0 * p->topk, c, st);
     if (rc) return rc;

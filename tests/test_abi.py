@@ -69,6 +69,19 @@ def test_host_validation_without_gpu():
                          scale=0.5, dtype="bf16")
     assert dsa.lib.dsa_sparse_attn_fwd(ctypes.byref(bf), 16, 16, 16, 16, 16, 16, None, None) == \
         dsa.DSA_ERR_UNSUPPORTED
+    # the FP8 indexer flag adds the E4M3 operands and scales to the forward's
+    # workspace; the scratch-free forward runs the bf16 indexer only
+    f8 = dsa.make_params(B=1, S_q=64, S_k=64, H=128, d_qk=576, d_v=512, H_I=64, d_I=128, topk=16,
+                         scale=0.5, dtype="bf16", flags=2)
+    plain = dsa.make_params(B=1, S_q=64, S_k=64, H=128, d_qk=576, d_v=512, H_I=64, d_I=128, topk=16,
+                            scale=0.5, dtype="bf16")
+    assert dsa.workspace_size(f8, dsa.DSA_CALL_FORWARD) >= \
+        dsa.workspace_size(plain, dsa.DSA_CALL_FORWARD) + 64 * 64 * 128 + 64 * 128 + 64 * 64 * 4 + 64 * 4
+    assert dsa.lib.dsa_forward_static_ws(ctypes.byref(f8), *([16] * 9), None) == dsa.DSA_ERR_UNSUPPORTED
+    fp32 = dsa.make_params(B=1, S_q=8, S_k=8, H=2, d_qk=8, d_v=4, H_I=2, d_I=4, topk=4, scale=0.5,
+                           dtype="fp32")
+    assert dsa.lib.dsa_indexer_scores_fp8(ctypes.byref(fp32), 16, 16, 16, 16, 16, 0, 1, 16, None) == \
+        dsa.DSA_ERR_UNSUPPORTED
     # the bf16 path stores O with TMA: q, kv and out must be 16-byte aligned
     ds = dsa.make_params(B=1, S_q=8, S_k=8, H=128, d_qk=576, d_v=512, H_I=64, d_I=128, topk=4,
                          scale=0.5, dtype="bf16")
