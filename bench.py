@@ -372,7 +372,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-bwd", action="store_true", help="skip the training-shape backward timing")
-    ap.add_argument("--stage", default=None, choices=["topk", "bwd"],
+    ap.add_argument("--stage", default=None, choices=["topk", "bwd", "fp8idx"],
                     help="time one stage alone (a profiling aid; prints its own JSON line)")
     args = ap.parse_args()
     wl = synth.WORKLOADS[args.workload]
@@ -394,6 +394,16 @@ def main():
     import sparse_attention_long_gb300 as dsa
     if args.stage == "topk":
         print(json.dumps(topk_stage(dsa, dev, wl, args.steps, args.warmup, load_peaks())), flush=True)
+        return
+    if args.stage == "fp8idx":
+        S0 = wl["S"]
+        xi = synth.make_inputs(wl, device=dev)
+        p0 = dsa.make_params(B=1, S_q=S0, S_k=S0, H=wl["H"], d_qk=wl["d_qk"], d_v=wl["d_v"], H_I=wl["H_I"],
+                             d_I=wl["d_I"], topk=wl["topk"], scale=wl["scale"], dtype="bf16")
+        W0 = dsa.wave_rows(p0)
+        wv = [(r0, min(W0, S0 - r0)) for r0 in range(0, S0, W0)]
+        r = fp8_indexer_stage(dsa, dev, wl, xi, wv, args.steps, load_peaks()["bf16_tflops"])
+        print(json.dumps(dict(stage="fp8idx", workload=wl["name"], **r)), flush=True)
         return
     if args.stage == "bwd":
         wname = args.workload if args.workload != "dsv32_S32768" else "dsv32_S16384_train"
