@@ -14,8 +14,8 @@
 //   scores  S, dP   per (token, 128-key tile) in TMEM; epilogue writes
 //           P = exp(scale*S - m)/l and scale*dS = scale*P*(dP - D)
 //   dq      dQ[t]   = (scale*dS) K_sel           per (token, 192-col tile)
-//   dkv     dKV_sel += (scale*dS)^T Q + P^T dO   per (token, key tile, col tile),
-//           scattered with fp32 vector reductions.
+//   dkv     dKV_sel += (scale*dS)^T Q + P^T dO   per (token, col tile), all key
+//           tiles, persistent; scattered with fp32 vector reductions.
 // The same scores kernel in its logits-only form gives the head-summed
 // attention probabilities the indexer KL loss needs (kl_tc.cu takes it from
 // there).
@@ -461,135 +461,230 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // --------------------------------- dkv --------------------------------------
-// CTA = (row, 128-key tile, column tile n: [0,256) | [256,512) | [512,576)).
-// D[128 keys x N] = (scale*dS)^T Q (+ P^T dO for value columns), contracted
-// over the 128 heads in eight chunks of 16 through a 3-stage TMA ring (96 KB of
-// shared memory, so two CTAs share an SM and one's reductions overlap the
-// other's loads and MMAs).  P and
-// scale*dS enter as bf16 pairs hi + lo (a single bf16 rounding of P or dS
-// would leave the accumulated dKV of early keys about 0.1 off at this size).
-// Both operands are MN-major straight from TMA boxes (64 keys or 64 columns
-// by 16 heads).  warp 1 lane 0: TMA; warp 0 lane 0: MMA; then all four warps
-// drain TMEM (thread = key) and scatter-add their rows into dkv with vector
-// reductions.
-constexpr int kVStages = 3;
-constexpr int kVHeads = 16;                 // heads per stage
+// Persistent: one CTA per SM walks work items (row, column tile nt: [0,256) |
+// [256,512) | [512,576)), item = 3 * row + nt, strided over the grid, so the
+// three column tiles of a row run on neighbouring CTAs at about the same time
+// and read the row's P / dS tiles once from HBM and twice from L2.
+//
+// Per item, D[128 keys x N] = (scale*dS)^T Q (+ P^T dO for value columns) for
+// every 128-key tile of the row, contracted over the 128 heads in eight
+// chunks of 16.  The B operands (q and dO columns of the item, 128 heads x N)
+// stay resident in shared memory for all key tiles; the A operands (dS^T and
+// P^T as bf16 pairs hi + lo, 128 keys x 16 heads; a single bf16 rounding of P
+// or dS would leave the accumulated dKV of early keys about 0.1 off) stream
+// through a 4-stage TMA ring.  Both operands are MN-major straight from TMA
+// boxes (64 keys or 64 columns by 16 heads).  Two TMEM accumulators of 256
+// columns let the four epilogue warps scatter key tile j (fp32 vector
+// reductions into dkv, full 128-byte line segments) while the MMAs of key
+// tile j + 1 run.  The next item's B chunks reload one by one as the MMAs of
+// the current item's last key tile release them.
+//
+// warp 0 lane 0: MMA issue; warp 1 lane 0: TMA; warps 2-5: TMEM drain and
+// scatter (warp w reads TMEM lanes 32 * (w % 4) ...).  Key tiles with no
+// valid id skip their loads and MMAs (the producer and the issuer derive the
+// same tile mask from the index row); the accumulator protocol still runs
+// for them and the epilogue adds nothing.
+constexpr int kVStages = 4;
+constexpr int kVHeads = 16;                 // heads per chunk
+constexpr int kVChunks = kH / kVHeads;      // 8
 constexpr int kVBox = 64 * kVHeads * 2;     // 2 KB: 64 keys (or columns) x 16 heads
+constexpr int kVThreads = 192;
 struct __align__(1024) DkvSmem {
+  uint8_t bq[kVChunks][4][kVBox];           // q columns of the item, [head chunk][64-column box]
+  uint8_t bo[kVChunks][4][kVBox];           // dO columns
   uint8_t a[kVStages][4][2][kVBox];         // [dS hi, dS lo, P hi, P lo][key half]
-  uint8_t bq[kVStages][4][kVBox];           // q columns, 4 boxes of 64
-  uint8_t bo[kVStages][4][kVBox];           // dO columns
-  int32_t idx[128];
-  uint32_t mask[4];
-  uint64_t full[kVStages], empty[kVStages], done;
+  uint8_t scratch[4][4096];                 // scatter transpose, one per epilogue warp
+  uint64_t afull[kVStages], aempty[kVStages], bfull[kVChunks], bempty[kVChunks];
+  uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem_base;
   int abort;
 };
 
-__global__ void __launch_bounds__(128, 2)
+// bit j: key tile j of the row holds at least one valid key id (warp-wide)
+__device__ __forceinline__ uint32_t dkv_tile_mask(const int32_t* __restrict__ idx_row, int k, int S_k) {
+  const int lane = threadIdx.x & 31;
+  uint32_t m = 0;
+#pragma unroll 16
+  for (int sl = lane; sl < k; sl += 32) {
+    const int id = idx_row[sl];
+    if (id >= 0 && id < S_k) m |= 1u << (sl >> 7);
+  }
+  return __reduce_or_sync(0xffffffffu, m);
+}
+
+__global__ void __launch_bounds__(kVThreads, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tm_ds, const __grid_constant__ CUtensorMap tm_dslo,
                const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_plo,
                const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                Shape s, const int32_t* __restrict__ idx, float* __restrict__ dkv, int ntile,
-               DevCtx c) {
+               long long nitems, DevCtx c) {
   extern __shared__ uint8_t smem_raw[];
   DkvSmem& sm = *reinterpret_cast<DkvSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nt = blockIdx.x % 3;
-  const int tile = (blockIdx.x / 3) % ntile;
-  const long long row = blockIdx.x / (3 * ntile);
-  const long long b = row / s.S_q;
   const int k = s.topk;
-  const int slot0 = tile * 128;
-  const int N = nt < 2 ? 256 : 64;
-  const int ncb = N / 64;
-  const bool withV = nt < 2;
-  const int nA = withV ? 4 : 2;             // A operands per stage
-  constexpr int nChunk = kH / kVHeads;
   volatile int* abort_flag = &sm.abort;
-  {
-    const int sl = slot0 + threadIdx.x;
-    int id = sl < k ? idx[row * k + sl] : -1;
-    if (id < 0 || id >= s.S_k) id = -1;
-    sm.idx[threadIdx.x] = id;
-    const uint32_t bal = __ballot_sync(0xffffffffu, id >= 0);
-    if (lane == 0) sm.mask[warp] = bal;
-  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kVStages; ++i) {
-      mbar_init(smem_u32(&sm.full[i]), 1);
-      mbar_init(smem_u32(&sm.empty[i]), 1);
+      mbar_init(smem_u32(&sm.afull[i]), 1);
+      mbar_init(smem_u32(&sm.aempty[i]), 1);
     }
-    mbar_init(smem_u32(&sm.done), 1);
+    for (int i = 0; i < kVChunks; ++i) {
+      mbar_init(smem_u32(&sm.bfull[i]), 1);
+      mbar_init(smem_u32(&sm.bempty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sm.acc_full[i]), 1);
+      mbar_init(smem_u32(&sm.acc_empty[i]), 4);
+    }
     sm.abort = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(smem_u32(&sm.tmem_base), 256);
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);
     tmem_relinquish();
     tc_fence_before();
   }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  const bool any = (sm.mask[0] | sm.mask[1] | sm.mask[2] | sm.mask[3]) != 0u;
-  if (any && warp == 1 && lane == 0) {
-    const CUtensorMap* am[4] = {&tm_ds, &tm_dslo, &tm_p, &tm_plo};
-    const uint32_t bytes = (uint32_t)(nA * 2 + (withV ? 2 : 1) * ncb) * kVBox;
-    for (int ch = 0; ch < nChunk; ++ch) {
-      const int st = ch % kVStages;
-      if (!mbar_wait(smem_u32(&sm.empty[st]), ((ch / kVStages) & 1) ^ 1, c, abort_flag)) break;
-      const uint32_t fb = smem_u32(&sm.full[st]);
-      mbar_arrive_expect_tx(fb, bytes);
-      const int y = (int)(row * kH) + kVHeads * ch;
-      for (int o = 0; o < nA; ++o)
-        for (int kk = 0; kk < 2; ++kk)
-          tma_load_2d(smem_u32(sm.a[st][o][kk]), am[o], slot0 + 64 * kk, y, fb);
-      for (int cb = 0; cb < ncb; ++cb) {
-        tma_load_2d(smem_u32(sm.bq[st][cb]), &tm_q, 256 * nt + 64 * cb, y, fb);
-        if (withV) tma_load_2d(smem_u32(sm.bo[st][cb]), &tm_do, 256 * nt + 64 * cb, y, fb);
-      }
-    }
-    for (int ch = nChunk - kVStages; ch < nChunk; ++ch)  // drain: no copy left in flight
-      mbar_wait(smem_u32(&sm.full[ch % kVStages]), (ch / kVStages) & 1, c, abort_flag);
-  } else if (any && warp == 0 && lane == 0) {
-    const uint32_t idesc = idesc_bf16(128, N, true, true);
-    for (int ch = 0; ch < nChunk; ++ch) {
-      const int st = ch % kVStages;
-      if (!mbar_wait(smem_u32(&sm.full[st]), (ch / kVStages) & 1, c, abort_flag)) break;
-      tc_fence_after();
-#pragma unroll 1
-      for (int o = 0; o < nA; ++o) {
-        const uint32_t a0 = smem_u32(sm.a[st][o][0]);
-        const uint32_t b0 = smem_u32(o < 2 ? sm.bq[st][0] : sm.bo[st][0]);
-#pragma unroll
-        for (int kk = 0; kk < kVHeads / 16; ++kk)
-          mma_bf16_ss(tmem, sdesc(a0 + kk * 2048, kVBox, 1024, kSw128),
-                      sdesc(b0 + kk * 2048, kVBox, 1024, kSw128), idesc,
-                      (ch > 0 || o > 0 || kk > 0) ? 1u : 0u);
-      }
-      mma_commit(smem_u32(&sm.empty[st]));
-    }
-    mma_commit(smem_u32(&sm.done));
-  }
-  if (any) {
-    const int key = warp * 32 + lane;
-    const bool have = mbar_wait_warp(smem_u32(&sm.done), 0, c, abort_flag);
-    tc_fence_after();
-    const int id = sm.idx[key];
-    float* dst = dkv + (b * s.S_k + (id < 0 ? 0 : id)) * (long long)kDQK + 256 * nt;
-#pragma unroll 1
-    for (int cc = 0; cc < N; cc += 32) {
-      uint32_t v[32];
-      if (have) {
-        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + cc, v);
-        tmem_ld_wait(v);
-        if (id >= 0) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            red_add_v4(dst + cc + i, __uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                       __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+  bool ok = true;
+  if (warp == 0) {
+    // ---- MMA issue ----
+    uint32_t ast = 0, g = 0, it = 0;
+    for (long long item = blockIdx.x; ok && item < nitems; item += gridDim.x, ++it) {
+      const long long row = item / 3;
+      const int nt = (int)(item % 3);
+      const uint32_t mask = dkv_tile_mask(idx + row * k, k, s.S_k);
+      if (lane == 0) {
+        const int N = nt < 2 ? 256 : 64;
+        const int nA = nt < 2 ? 4 : 2;
+        const uint32_t idesc = idesc_bf16(128, N, true, true);
+        // B chunk ch is awaited at the first valid tile j0, in the order the
+        // producer issues it (B chunk ch, then tile j0's A chunk ch), and
+        // released after its last reader (chunk ch of the last valid tile
+        // jl).  Commits only follow MMAs: a tile without MMAs arrives on its
+        // accumulator barrier directly.
+        const int j0 = mask ? __ffs(mask) - 1 : -1;
+        const int jl = mask ? 31 - __clz(mask) : -1;
+        for (int ch = 0; ok && jl < 0 && ch < kVChunks; ++ch) {  // no valid tile: B unused
+          ok = mbar_wait(smem_u32(&sm.bfull[ch]), it & 1, c, abort_flag);
+          if (ok) mbar_arrive(smem_u32(&sm.bempty[ch]));
         }
+        for (int j = 0; ok && j < ntile; ++j, ++g) {
+          const uint32_t buf = g & 1;
+          ok = mbar_wait(smem_u32(&sm.acc_empty[buf]), ((g >> 1) & 1) ^ 1, c, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const bool valid = (mask >> j) & 1u;
+          const uint32_t d = tmem + buf * 256;
+          bool first = true;
+          for (int ch = 0; valid && ch < kVChunks; ++ch) {
+            if (j == j0) {
+              ok = mbar_wait(smem_u32(&sm.bfull[ch]), it & 1, c, abort_flag);
+              if (!ok) break;
+            }
+            const uint32_t st = ast % kVStages;
+            ok = mbar_wait(smem_u32(&sm.afull[st]), (ast / kVStages) & 1, c, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int o = 0; o < nA; ++o) {
+              const uint32_t a0 = smem_u32(sm.a[st][o][0]);
+              const uint32_t b0 = smem_u32(o < 2 ? sm.bq[ch][0] : sm.bo[ch][0]);
+              mma_bf16_ss(d, sdesc(a0, kVBox, 1024, kSw128), sdesc(b0, kVBox, 1024, kSw128), idesc,
+                          first ? 0u : 1u);
+              first = false;
+            }
+            mma_commit(smem_u32(&sm.aempty[st]));
+            ++ast;
+            if (j == jl) mma_commit(smem_u32(&sm.bempty[ch]));
+          }
+          if (!ok) break;
+          if (valid) mma_commit(smem_u32(&sm.acc_full[buf]));
+          else mbar_arrive(smem_u32(&sm.acc_full[buf]));  // nothing to read: the epilogue skips it
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+  } else if (warp == 1) {
+    // ---- TMA: B chunks once per item, A chunks per valid key tile ----
+    const CUtensorMap* am[4] = {&tm_ds, &tm_dslo, &tm_p, &tm_plo};
+    uint32_t ast = 0, it = 0;
+    for (long long item = blockIdx.x; ok && item < nitems; item += gridDim.x, ++it) {
+      const long long row = item / 3;
+      const int nt = (int)(item % 3);
+      const uint32_t mask = dkv_tile_mask(idx + row * k, k, s.S_k);
+      if (lane == 0) {
+        const bool withV = nt < 2;
+        const int ncb = withV ? 4 : 1;
+        const int nA = withV ? 4 : 2;
+        const uint32_t bytesA = (uint32_t)(nA * 2) * kVBox;
+        const uint32_t bytesB = (uint32_t)((withV ? 2 : 1) * ncb) * kVBox;
+        const int y0 = (int)(row * kH);
+        auto load_a = [&](int j, int ch) -> bool {
+          const uint32_t st = ast % kVStages;
+          if (!mbar_wait(smem_u32(&sm.aempty[st]), ((ast / kVStages) & 1) ^ 1, c, abort_flag)) return false;
+          const uint32_t fb = smem_u32(&sm.afull[st]);
+          mbar_arrive_expect_tx(fb, bytesA);
+          for (int o = 0; o < nA; ++o)
+            for (int kk = 0; kk < 2; ++kk)
+              tma_load_2d(smem_u32(sm.a[st][o][kk]), am[o], j * 128 + 64 * kk, y0 + kVHeads * ch, fb);
+          ++ast;
+          return true;
+        };
+        const int j0 = mask ? __ffs(mask) - 1 : -1;
+        for (int ch = 0; ok && ch < kVChunks; ++ch) {
+          ok = mbar_wait(smem_u32(&sm.bempty[ch]), (it & 1) ^ 1, c, abort_flag);
+          if (!ok) break;
+          const uint32_t fb = smem_u32(&sm.bfull[ch]);
+          mbar_arrive_expect_tx(fb, bytesB);
+          for (int cb = 0; cb < ncb; ++cb) {
+            tma_load_2d(smem_u32(sm.bq[ch][cb]), &tm_q, 256 * nt + 64 * cb, y0 + kVHeads * ch, fb);
+            if (withV) tma_load_2d(smem_u32(sm.bo[ch][cb]), &tm_do, 256 * nt + 64 * cb, y0 + kVHeads * ch, fb);
+          }
+          if (j0 >= 0) ok = load_a(j0, ch);
+        }
+        for (int j = j0 + 1; ok && j0 >= 0 && j < ntile; ++j)
+          if ((mask >> j) & 1u)
+            for (int ch = 0; ok && ch < kVChunks; ++ch) ok = load_a(j, ch);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+  } else {
+    // ---- TMEM drain and scatter: thread = key of the tile ----
+    const int quad = warp & 3;
+    const uint32_t scratch = smem_u32(sm.scratch[warp - 2]);
+    uint32_t g = 0;
+    for (long long item = blockIdx.x; ok && item < nitems; item += gridDim.x) {
+      const long long row = item / 3;
+      const int nt = (int)(item % 3);
+      const int N = nt < 2 ? 256 : 64;
+      const long long b = row / s.S_q;
+      for (int j = 0; ok && j < ntile; ++j, ++g) {
+        const uint32_t buf = g & 1;
+        const int sl = j * 128 + quad * 32 + lane;
+        int id = sl < k ? idx[row * k + sl] : -1;
+        if (id >= s.S_k) id = -1;
+        ok = mbar_wait_warp(smem_u32(&sm.acc_full[buf]), (g >> 1) & 1, c, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, id >= 0)) {
+          float* dst = id < 0 ? nullptr : dkv + (b * s.S_k + id) * (long long)kDQK + 256 * nt;
+          const uint32_t taddr = tmem + buf * 256 + ((uint32_t)(quad * 32) << 16);
+#pragma unroll 1
+          for (int cc = 0; cc < N; cc += 64) {
+            uint32_t v[32], w[32];
+            tmem_ld32(taddr + cc, v);
+            tmem_ld32(taddr + cc + 32, w);
+            tmem_ld_wait(v);
+            tmem_ld_also(w);
+            warp_scatter_add_32x32(scratch, v, dst == nullptr ? nullptr : dst + cc);
+            warp_scatter_add_32x32(scratch, w, dst == nullptr ? nullptr : dst + cc + 32);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.acc_empty[buf]));
       }
     }
   }
@@ -597,7 +692,7 @@ __global__ void __launch_bounds__(128, 2)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -665,8 +760,13 @@ int launch_attn_bwd_tc(const Shape& s, const void* q, const void* kv, const int3
       ntile, c);
   dq_kernel<<<(unsigned)(rows * 3), 192, s2, st>>>(tds, tdslo, (const __nv_bfloat16*)kv, s, idx,
                                                     (__nv_bfloat16*)dq, c);
-  dkv_kernel<<<(unsigned)(rows * ntile * 3), 128, s3, st>>>(tds2, tdslo2, tp2, tplo2, tq2, tdo2, s,
-                                                             idx, dkv, ntile, c);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return DSA_ERR_CUDA;
+  const long long nitems = rows * 3;
+  dkv_kernel<<<(unsigned)(nitems < sms ? nitems : sms), kVThreads, s3, st>>>(
+      tds2, tdslo2, tp2, tplo2, tq2, tdo2, s, idx, dkv, ntile, nitems, c);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

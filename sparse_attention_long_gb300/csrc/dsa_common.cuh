@@ -329,6 +329,41 @@ __device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c
                : "memory");
 }
 
+// Scatter-add of a warp's 32 rows x 32 fp32 columns: lane i holds row i's 32
+// values (as a 32x32b TMEM load leaves them) and the address they add into
+// (row_dst, nullptr to skip the row).  The block is transposed through a 4 KB
+// warp-private shared scratch (16-byte chunks XOR-swizzled by row, so both
+// the row-wise stores and the column-wise loads are conflict-free), so each
+// reduction instruction covers four rows' whole 128-byte segments: L2 takes
+// full-line vector reductions at about twice the rate of 32 rows' 16-byte
+// pieces.  The caller owns the scratch for the duration of the call.
+__device__ __forceinline__ void warp_scatter_add_32x32(uint32_t scratch, const uint32_t (&v)[32],
+                                                       float* row_dst) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(scratch + lane * 128 + ((j ^ (lane & 7)) << 4)),
+                 "r"(v[4 * j]), "r"(v[4 * j + 1]), "r"(v[4 * j + 2]), "r"(v[4 * j + 3])
+                 : "memory");
+  __syncwarp();
+  const int ch = lane & 7;
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    const int r = 4 * p + (lane >> 3);
+    float* d = reinterpret_cast<float*>(
+        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(row_dst), r));
+    uint32_t x0, x1, x2, x3;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                 : "r"(scratch + r * 128 + ((ch ^ (r & 7)) << 4))
+                 : "memory");
+    if (d != nullptr)
+      red_add_v4(d + 4 * ch, __uint_as_float(x0), __uint_as_float(x1), __uint_as_float(x2),
+                 __uint_as_float(x3));
+  }
+  __syncwarp();
+}
+
 // Shared-memory matrix descriptor (tcgen05): start, leading / stride byte
 // offsets, fixed version 1, swizzle layout (0 none, 2 = 128B, 4 = 64B, 6 = 32B).
 constexpr uint32_t kSw128 = 2, kSw64 = 4;

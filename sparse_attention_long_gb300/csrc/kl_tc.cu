@@ -314,18 +314,17 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (tile + 1 < ntile) gather(tile + 1);  // the key tile is free once dq^T is done
       // scatter this key's dk_I row
       const int id = valid ? sm.idx[sl] : -1;
-      float* dst = dk_I + (b * s.S_k + (id < 0 ? 0 : id)) * (long long)kDI;
+      float* dst = id < 0 ? nullptr : dk_I + (b * s.S_k + id) * (long long)kDI;
+      // this warp's 32 rows of the dS^T hi buffer are its own until it
+      // writes the next tile's dS^T (the MMAs that read them are done): they
+      // serve as the transpose scratch of the scatter
+      const uint32_t scratch = smem_u32(sm.ds[0]) + quad * 4096;
 #pragma unroll 1
       for (int cc = 0; cc < kDI; cc += 32) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_off + kColDK + cc, v);
         tmem_ld_wait(v);
-        if (id >= 0) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            red_add_v4(dst + cc + i, __uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                       __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
-        }
+        warp_scatter_add_32x32(scratch, v, dst == nullptr ? nullptr : dst + cc);
       }
       tc_fence_before();
     }
