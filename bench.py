@@ -136,28 +136,32 @@ def fp8_indexer_stage(dsa, dev, wl, x, waves, steps, peak_tc):
             "note": "E4M3 q_I, k_I with one fp32 scale per 128-vector; outside the timed step"}
 
 
-def backward_stage(dsa, dev, steps, peak_tc, workload="dsv32_S16384_train"):
+def backward_stage(dsa, dev, steps, peak_tc, workload="dsv32_S16384_train", rows=None):
     """The training-shape backward (S = 16384, top-2048, all rows): the forward,
     the attention backward (dq, dkv), the indexer KL-loss backward, each timed
     alone, and dsa_backward (both in one call sharing the recompute of P).
-    `workload` picks another shape (a smaller one for profiling)."""
+    `workload` picks another shape and `rows` the last `rows` query rows
+    against all S keys (a context-parallel shard), for profiling on a small
+    device footprint."""
     wl = synth.WORKLOADS[workload]
     S, k, H = wl["S"], wl["topk"], wl["H"]
-    x = synth.make_inputs(wl, device=dev, with_dout=True)
-    p = dsa.make_params(B=1, S_q=S, S_k=S, H=H, d_qk=wl["d_qk"], d_v=wl["d_v"], H_I=wl["H_I"],
-                        d_I=wl["d_I"], topk=k, scale=wl["scale"], dtype="bf16")
+    S_q = S if rows is None else int(rows)
+    x = synth.make_inputs(wl, device=dev, with_dout=True, S_q=S_q)
+    p = dsa.make_params(B=1, S_q=S_q, S_k=S, H=H, d_qk=wl["d_qk"], d_v=wl["d_v"], H_I=wl["H_I"],
+                        d_I=wl["d_I"], topk=k, scale=wl["scale"], dtype="bf16",
+                        q_row_offset=S - S_q)
     ring = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_FORWARD), dtype=torch.uint8, device=dev)
-    idx = torch.empty(1, S, k, dtype=torch.int32, device=dev)
-    out = torch.empty(1, S, H, wl["d_v"], dtype=torch.bfloat16, device=dev)
-    m = torch.empty(1, S, H, device=dev)
+    idx = torch.empty(1, S_q, k, dtype=torch.int32, device=dev)
+    out = torch.empty(1, S_q, H, wl["d_v"], dtype=torch.bfloat16, device=dev)
+    m = torch.empty(1, S_q, H, device=dev)
     l = torch.empty_like(m)
-    dq = torch.empty(1, S, H, wl["d_qk"], dtype=torch.bfloat16, device=dev)
+    dq = torch.empty(1, S_q, H, wl["d_qk"], dtype=torch.bfloat16, device=dev)
     dkv = torch.zeros(1, S, wl["d_qk"], device=dev)
     ws_b = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_ATTN_BWD), dtype=torch.uint8, device=dev)
     loss = torch.zeros(1, device=dev)
-    dq_I = torch.empty(1, S, wl["H_I"], wl["d_I"], dtype=torch.bfloat16, device=dev)
+    dq_I = torch.empty(1, S_q, wl["H_I"], wl["d_I"], dtype=torch.bfloat16, device=dev)
     dk_I = torch.zeros(1, S, wl["d_I"], device=dev)
-    dw = torch.empty(1, S, wl["H_I"], device=dev)
+    dw = torch.empty(1, S_q, wl["H_I"], device=dev)
     ws_k = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_KL_BWD), dtype=torch.uint8, device=dev)
     ws_all = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_BACKWARD), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -172,8 +176,8 @@ def backward_stage(dsa, dev, steps, peak_tc, workload="dsv32_S16384_train"):
     t_kl = time_calls(kl, steps, 1, stream)
     t_both = time_calls(both, steps, 1, stream)
     assert dsa.get_status() == 0, "device status after the backward"
-    f_bwd, f_kl = algorithmic_bwd(wl, np.arange(S))
-    return {"workload": wl["name"], "calls_timed": steps,
+    f_bwd, f_kl = algorithmic_bwd(wl, np.arange(S - S_q, S))
+    return {"workload": wl["name"], "rows": S_q, "calls_timed": steps,
             "forward_ms": t_fwd, "attn_bwd_ms": t_bwd, "kl_bwd_ms": t_kl,
             "backward_ms": t_both,
             "backward_tflops": (f_bwd + f_kl) / (t_both * 1e-3) / 1e12,
@@ -372,6 +376,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-bwd", action="store_true", help="skip the training-shape backward timing")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="with --stage bwd: the last N query rows against all keys (profiling)")
     ap.add_argument("--stage", default=None, choices=["topk", "bwd", "fp8idx"],
                     help="time one stage alone (a profiling aid; prints its own JSON line)")
     args = ap.parse_args()
@@ -407,7 +413,8 @@ def main():
         return
     if args.stage == "bwd":
         wname = args.workload if args.workload != "dsv32_S32768" else "dsv32_S16384_train"
-        bwd = backward_stage(dsa, dev, args.steps, load_peaks()["bf16_tflops_sustained"], wname)
+        bwd = backward_stage(dsa, dev, args.steps, load_peaks()["bf16_tflops_sustained"], wname,
+                             args.rows)
         print(json.dumps(dict(stage="bwd", **bwd)), flush=True)
         return
 

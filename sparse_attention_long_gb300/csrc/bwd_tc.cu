@@ -479,8 +479,9 @@ __global__ void __launch_bounds__(192, 1)
 // tile j + 1 run.  The next item's B chunks reload one by one as the MMAs of
 // the current item's last key tile release them.
 //
-// warp 0 lane 0: MMA issue; warp 1 lane 0: TMA; warps 2-5: TMEM drain and
-// scatter (warp w reads TMEM lanes 32 * (w % 4) ...).  Key tiles with no
+// warp 0 lane 0: MMA issue; warp 1 lane 0: TMA; warps 2-9: TMEM drain and
+// scatter (warp w reads TMEM lanes 32 * (w % 4) ..., half (w - 2) / 4 of the
+// item's columns: eight warps keep enough reductions in flight).  Key tiles with no
 // valid id skip their loads and MMAs (the producer and the issuer derive the
 // same tile mask from the index row); the accumulator protocol still runs
 // for them and the epilogue adds nothing.
@@ -488,17 +489,19 @@ constexpr int kVStages = 4;
 constexpr int kVHeads = 16;                 // heads per chunk
 constexpr int kVChunks = kH / kVHeads;      // 8
 constexpr int kVBox = 64 * kVHeads * 2;     // 2 KB: 64 keys (or columns) x 16 heads
-constexpr int kVThreads = 192;
+constexpr int kVThreads = 320;
+constexpr int kVEpiWarps = 8;
 struct __align__(1024) DkvSmem {
   uint8_t bq[kVChunks][4][kVBox];           // q columns of the item, [head chunk][64-column box]
   uint8_t bo[kVChunks][4][kVBox];           // dO columns
   uint8_t a[kVStages][4][2][kVBox];         // [dS hi, dS lo, P hi, P lo][key half]
-  uint8_t scratch[4][4096];                 // scatter transpose, one per epilogue warp
+  uint8_t scratch[kVEpiWarps][4096];        // scatter transpose, one per epilogue warp
   uint64_t afull[kVStages], aempty[kVStages], bfull[kVChunks], bempty[kVChunks];
   uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(DkvSmem) + 1024 <= 232448, "dkv shared memory");
 
 // bit j: key tile j of the row holds at least one valid key id (warp-wide)
 __device__ __forceinline__ uint32_t dkv_tile_mask(const int32_t* __restrict__ idx_row, int k, int S_k) {
@@ -534,7 +537,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sm.acc_full[i]), 1);
-      mbar_init(smem_u32(&sm.acc_empty[i]), 4);
+      mbar_init(smem_u32(&sm.acc_empty[i]), kVEpiWarps);
     }
     sm.abort = 0;
     fence_mbar_init();
@@ -652,7 +655,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
     }
   } else {
     // ---- TMEM drain and scatter: thread = key of the tile ----
-    const int quad = warp & 3;
+    const int quad = warp & 3, half = (warp - 2) >> 2;
     const uint32_t scratch = smem_u32(sm.scratch[warp - 2]);
     uint32_t g = 0;
     for (long long item = blockIdx.x; ok && item < nitems; item += gridDim.x) {
@@ -671,15 +674,19 @@ __global__ void __launch_bounds__(kVThreads, 1)
         if (__any_sync(0xffffffffu, id >= 0)) {
           float* dst = id < 0 ? nullptr : dkv + (b * s.S_k + id) * (long long)kDQK + 256 * nt;
           const uint32_t taddr = tmem + buf * 256 + ((uint32_t)(quad * 32) << 16);
+          const int c1 = (half + 1) * (N / 2);
 #pragma unroll 1
-          for (int cc = 0; cc < N; cc += 64) {
+          for (int cc = half * (N / 2); cc < c1; cc += 64) {
+            const bool two = cc + 32 < c1;
             uint32_t v[32], w[32];
             tmem_ld32(taddr + cc, v);
-            tmem_ld32(taddr + cc + 32, w);
+            if (two) tmem_ld32(taddr + cc + 32, w);
             tmem_ld_wait(v);
-            tmem_ld_also(w);
             warp_scatter_add_32x32(scratch, v, dst == nullptr ? nullptr : dst + cc);
-            warp_scatter_add_32x32(scratch, w, dst == nullptr ? nullptr : dst + cc + 32);
+            if (two) {
+              tmem_ld_also(w);
+              warp_scatter_add_32x32(scratch, w, dst == nullptr ? nullptr : dst + cc + 32);
+            }
           }
         }
         tc_fence_before();

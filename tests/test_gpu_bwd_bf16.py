@@ -15,9 +15,10 @@ from gpu_util import DEV, bf16_close, lib, np64, params
 pytestmark = pytest.mark.gpu
 
 
-def _run_case(wl, rows):
+def _run_case(wl, rows, edit=None):
     """Oracle forward on `rows` (global positions) of workload `wl`, then the
-    backward on both sides.  The q-side inputs are drawn for len(rows) rows."""
+    backward on both sides.  The q-side inputs are drawn for len(rows) rows;
+    `edit(idx)` may rewrite the index sets in place before either side runs."""
     n, S, k = len(rows), wl["S"], wl["topk"]
     x = synth.make_inputs(wl, with_dout=True, S_q=n)
     pos = oracle.positions(1, n, q_row_index=np.asarray(rows))
@@ -28,6 +29,8 @@ def _run_case(wl, rows):
         row = idx[0, r].copy()
         rng.shuffle(row)
         idx[0, r] = row
+    if edit is not None:
+        edit(idx)
     O, m, l = oracle.sparse_attn_fwd(x["q"], x["kv"], idx, wl["scale"], wl["d_v"])
     O16 = torch.as_tensor(O).to(torch.bfloat16)
     m32 = torch.as_tensor(m).float()
@@ -100,3 +103,22 @@ def test_backward_train_shape_sampled_rows():
     rows = sorted(set([0, 1, 2047, 2048, 2049, 8191, S - 2, S - 1] +
                       np.random.default_rng(5).integers(0, S, 8).tolist()))
     _check(_run_case(wl, rows))
+
+
+def test_backward_empty_rows_and_late_key_tiles():
+    # k = 256 (two key tiles): some rows select nothing at all, others hold
+    # their keys only in the second tile (the first tile is all holes), so
+    # the dKV pass meets items with no valid tile and items whose first
+    # valid tile is not the first one
+    wl = dict(synth.v32(448, "dsv32_S448"), topk=256)
+
+    def edit(idx):
+        for r in range(idx.shape[1]):
+            if r % 7 == 3:
+                idx[0, r] = -1
+            elif r % 7 == 5:
+                keep = idx[0, r][idx[0, r] >= 0][:128]
+                idx[0, r] = -1
+                idx[0, r, 256 - keep.size:] = keep
+
+    _check(_run_case(wl, list(range(448)), edit))
