@@ -72,8 +72,11 @@ enum { DSA_CP_COLOSSAL = 0, DSA_CP_ULYSSES = 1 };
 /* dsa_params.flags: DSA_FLAG_CAUSAL_ONLY: dsa_indexer_scores(_fp8) writes
  * only the causal entries s <= pos(t) and leaves the rest of each score row
  * untouched.  DSA_FLAG_FP8_INDEXER: dsa_forward scores with the FP8 (E4M3)
- * indexer of dsa_indexer_scores_fp8 (DeepSeek indexer shapes, bf16). */
-enum { DSA_FLAG_CAUSAL_ONLY = 1, DSA_FLAG_FP8_INDEXER = 2 };
+ * indexer of dsa_indexer_scores_fp8 (DeepSeek indexer shapes, bf16).
+ * DSA_FLAG_FUSED_TOPK: dsa_forward selects through dsa_indexer_topk (the
+ * fused indexer + streaming top-k; bf16 DeepSeek indexer shapes, S_k < 65536,
+ * not with DSA_FLAG_FP8_INDEXER); the indices are the same. */
+enum { DSA_FLAG_CAUSAL_ONLY = 1, DSA_FLAG_FP8_INDEXER = 2, DSA_FLAG_FUSED_TOPK = 4 };
 
 /* workspace queries (dsa_workspace_size `which`) */
 enum {
@@ -81,7 +84,8 @@ enum {
   DSA_CALL_ATTN_FWD = 1,
   DSA_CALL_ATTN_BWD = 2,
   DSA_CALL_KL_BWD = 3,
-  DSA_CALL_BACKWARD = 4
+  DSA_CALL_BACKWARD = 4,
+  DSA_CALL_INDEXER_TOPK = 5
 };
 
 typedef struct {
@@ -167,6 +171,26 @@ int dsa_indexer_scores_fp8(const dsa_params *p, const uint8_t *q8, const float *
  */
 int dsa_topk(const dsa_params *p, const float *scores, int64_t row_begin, int64_t rows,
              int32_t *idx, dsa_stream_t stream);
+
+/*
+ * Fused Lightning Indexer + streaming top-k (the pages select "Top-k
+ * positions of each token" inside the indexer stage: [DSA-32K] "DSA fused
+ * ops", Lightning Indexer forward; [NPU-ops] "DSA").  For flattened rows
+ * [row_begin, row_begin+rows) writes idx[(r - row_begin)*topk ...] exactly as
+ * dsa_indexer_scores followed by dsa_topk would (same scores, same order key,
+ * ascending indices, -1 tail), without a score matrix: while the indexer
+ * streams a row's keys it keeps a running threshold no larger than the row's
+ * k-th largest score seen so far and writes out only the keys at or above it
+ * (key and position, 8 bytes each); an exact selection over those candidates
+ * follows.  bf16 DeepSeek indexer shapes (H_I 64, d_I 128), S_k < 65536;
+ * otherwise DSA_ERR_UNSUPPORTED.
+ *   workspace: dsa_workspace_size(p, DSA_CALL_INDEXER_TOPK) bytes (candidate
+ *   lists for one wave of wave_rows rows: 8 x wave_rows x S_k bytes plus
+ *   counts), 16-byte aligned; the rows go through it in waves.
+ */
+int dsa_indexer_topk(const dsa_params *p, const void *q_I, const void *k_I, const void *w,
+                     int64_t row_begin, int64_t rows, int32_t *idx, void *workspace,
+                     dsa_stream_t stream);
 
 /*
  * Sparse multi-query attention forward.  [DSA-32K] Sparse Flash Attention
@@ -268,6 +292,8 @@ int dsa_backward(const dsa_params *p, const void *q, const void *kv, const int32
 int dsa_forward(const dsa_params *p, const void *q_I, const void *k_I, const void *w,
                 const void *q, const void *kv, int32_t *idx_out, void *out, float *softmax_max,
                 float *softmax_sum, void *workspace, dsa_stream_t stream);
+/* (dsa_forward with DSA_FLAG_FUSED_TOPK: the indexer and top-k of each wave
+ * are dsa_indexer_topk's, and the workspace holds its candidate lists.) */
 
 /*
  * Whole forward with no workspace argument (this library's own addition; the
@@ -282,7 +308,7 @@ int dsa_forward(const dsa_params *p, const void *q_I, const void *k_I, const voi
  * only if the device's CUDA context changed since.  All calls share the ring:
  * calls that overlap on the GPU race on it.
  * Returns DSA_ERR_UNSUPPORTED when S_k > 2,097,152 (4 score rows would not
- * fit the ring) or with DSA_FLAG_FP8_INDEXER (bf16 indexer only); never
+ * fit the ring) or with DSA_FLAG_FP8_INDEXER or DSA_FLAG_FUSED_TOPK; never
  * allocates or frees device memory.
  */
 int dsa_forward_static_ws(const dsa_params *p, const void *q_I, const void *k_I, const void *w,

@@ -21,7 +21,8 @@ DSA_BSND, DSA_TND = 0, 1
 DSA_BF16, DSA_FP32 = 0, 1
 DSA_CP_COLOSSAL, DSA_CP_ULYSSES = 0, 1
 DSA_CALL_FORWARD, DSA_CALL_ATTN_FWD, DSA_CALL_ATTN_BWD, DSA_CALL_KL_BWD, DSA_CALL_BACKWARD = 0, 1, 2, 3, 4
-DSA_FLAG_CAUSAL_ONLY = 1
+DSA_CALL_INDEXER_TOPK = 5
+DSA_FLAG_CAUSAL_ONLY, DSA_FLAG_FP8_INDEXER, DSA_FLAG_FUSED_TOPK = 1, 2, 4
 
 _ERRNAMES = {0: "DSA_OK", -1: "DSA_ERR_INVALID_ARG", -2: "DSA_ERR_UNSUPPORTED",
              -3: "DSA_ERR_WORKSPACE", -4: "DSA_ERR_CUDA", -5: "DSA_ERR_TIMEOUT", -6: "DSA_ERR_INDEX"}
@@ -58,6 +59,7 @@ _sigs = {
     "dsa_indexer_quantize_fp8": ([_P] + [_vp] * 7, ctypes.c_int),
     "dsa_indexer_scores_fp8": ([_P, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp], ctypes.c_int),
     "dsa_topk": ([_P, _vp, _i64, _i64, _vp, _vp], ctypes.c_int),
+    "dsa_indexer_topk": ([_P, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp], ctypes.c_int),
     "dsa_sparse_attn_fwd": ([_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
     "dsa_sparse_attn_bwd": ([_P] + [_vp] * 11, ctypes.c_int),
     "dsa_indexer_kl_loss_bwd": ([_P] + [_vp] * 14, ctypes.c_int),
@@ -113,9 +115,12 @@ def make_params(*, B, S_q, S_k, H, d_qk, d_v, H_I, d_I, topk, scale, dtype="bf16
 
 
 def wave_rows(p: dsa_params) -> int:
-    """Rows per indexer/top-k wave dsa_forward uses: its score ring holds one
-    wave of S_k fp32 scores per row, so the library's workspace size gives it."""
-    return workspace_size(p, DSA_CALL_FORWARD) // (4 * p.S_k)
+    """Rows per indexer/top-k wave dsa_forward uses: its plain score ring holds
+    one wave of S_k fp32 scores per row, so the library's workspace size for
+    the same shape without the indexer flags gives it."""
+    q = dsa_params.from_buffer_copy(p)
+    q.flags &= ~(DSA_FLAG_FP8_INDEXER | DSA_FLAG_FUSED_TOPK)
+    return workspace_size(q, DSA_CALL_FORWARD) // (4 * q.S_k)
 
 
 def version() -> int:
@@ -146,6 +151,13 @@ def indexer_scores_fp8(p, q8, q_scale, k8, k_scale, w, row_begin, rows, scores, 
 def topk(p, scores, row_begin, rows, idx, stream=None):
     _chk(lib.dsa_topk(ctypes.byref(p), _ptr(scores), row_begin, rows, _ptr(idx), _stream(stream)),
          "dsa_topk")
+
+
+def indexer_topk(p, q_I, k_I, w, row_begin, rows, idx, workspace, stream=None):
+    """Fused indexer + streaming top-k: the indices dsa_indexer_scores +
+    dsa_topk give, without a score matrix (workspace: DSA_CALL_INDEXER_TOPK)."""
+    _chk(lib.dsa_indexer_topk(ctypes.byref(p), _ptr(q_I), _ptr(k_I), _ptr(w), row_begin, rows,
+                              _ptr(idx), _ptr(workspace), _stream(stream)), "dsa_indexer_topk")
 
 
 def sparse_attn_fwd(p, q, kv, idx, out, softmax_max, softmax_sum, workspace=None, stream=None):

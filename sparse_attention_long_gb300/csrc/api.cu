@@ -36,6 +36,12 @@ int launch_indexer_f8(const Shape& s, const uint8_t* q8, const float* q_scale, c
 int launch_indexer_tc(const Shape& s, const void* q_I, const void* k_I, const void* w,
                       long long row_begin, long long rows, float* scores, long long ld, DevCtx c,
                       cudaStream_t st);
+int launch_indexer_topk_tc(const Shape& s, const void* q_I, const void* k_I, const void* w,
+                           long long row_begin, long long rows, uint32_t* cand_key, int32_t* cand_pos,
+                           uint32_t* cand_cnt, long long ld, DevCtx c, cudaStream_t st);
+int launch_topk_cand(const Shape& s, const uint32_t* cand_key, const int32_t* cand_pos,
+                     const uint32_t* cand_cnt, long long ld, long long row_begin, long long rows,
+                     int32_t* idx, DevCtx c, cudaStream_t st);
 int launch_attn_fwd_tc(const Shape& s, const void* q, const void* kv, const int32_t* idx, void* out,
                        float* mx, float* sm, DevCtx c, cudaStream_t st);
 size_t bwd_tc_workspace(const Shape& s);
@@ -284,6 +290,37 @@ static long long wave_rows(const dsa_params* p) {
   return w < total ? w : total;
 }
 
+// The fused indexer + top-k: bf16 DeepSeek indexer shapes, S_k < 65536
+// (16-bit histogram counts).  Its workspace holds one wave's candidate lists:
+// keys [W][S_k] u32 | positions [W][S_k] i32 | counts [W] u32.
+static bool fused_topk_shape(const dsa_params* p) {
+  return p->dtype == DSA_BF16 && tc_indexer_shape(p) && p->S_k < 65536 &&
+         (p->flags & DSA_FLAG_FP8_INDEXER) == 0;
+}
+static size_t fused_list_bytes(const dsa_params* p) {
+  return align256((size_t)wave_rows(p) * (size_t)p->S_k * 4);
+}
+static size_t fused_topk_workspace(const dsa_params* p) {
+  return 2 * fused_list_bytes(p) + align256((size_t)wave_rows(p) * 4);
+}
+// rows [row_begin, row_begin + rows) in waves of wave_rows
+static int indexer_topk_waves(const dsa_params* p, const Shape& s, const void* q_I, const void* k_I,
+                              const void* w, long long row_begin, long long rows, int32_t* idx,
+                              void* workspace, DevCtx c, cudaStream_t st) {
+  const long long W = wave_rows(p);
+  uint32_t* ck = (uint32_t*)workspace;
+  int32_t* cp = (int32_t*)((uint8_t*)workspace + fused_list_bytes(p));
+  uint32_t* cc = (uint32_t*)((uint8_t*)workspace + 2 * fused_list_bytes(p));
+  for (long long r0 = row_begin; r0 < row_begin + rows; r0 += W) {
+    const long long n = (row_begin + rows - r0) < W ? (row_begin + rows - r0) : W;
+    int rc = launch_indexer_topk_tc(s, q_I, k_I, w, r0, n, ck, cp, cc, p->S_k, c, st);
+    if (rc) return rc;
+    rc = launch_topk_cand(s, ck, cp, cc, p->S_k, r0, n, idx + (r0 - row_begin) * p->topk, c, st);
+    if (rc) return rc;
+  }
+  return DSA_OK;
+}
+
 }  // namespace dsa
 
 using namespace dsa;
@@ -296,10 +333,12 @@ size_t dsa_workspace_size(const dsa_params* p, int which) {
   Shape s;
   if (check_params(p, &s) != DSA_OK) return 0;
   if (which == DSA_CALL_FORWARD) {
+    if (p->flags & DSA_FLAG_FUSED_TOPK) return fused_topk_shape(p) ? fused_topk_workspace(p) : 0;
     size_t bytes = (size_t)wave_rows(p) * (size_t)p->S_k * sizeof(float);
     if (p->flags & DSA_FLAG_FP8_INDEXER) bytes = align256(bytes) + fp8_buffers(p).total;
     return bytes;
   }
+  if (which == DSA_CALL_INDEXER_TOPK) return fused_topk_shape(p) ? fused_topk_workspace(p) : 0;
   if (which == DSA_CALL_ATTN_BWD && tc_bwd_shape(p)) return bwd_tc_workspace(s);
   if (which == DSA_CALL_KL_BWD && tc_bwd_shape(p) && tc_indexer_shape(p)) return kl_tc_workspace(s);
   if (which == DSA_CALL_BACKWARD) {
@@ -328,6 +367,23 @@ int dsa_indexer_scores(const dsa_params* p, const void* q_I, const void* k_I, co
   const bool fill = (p->flags & DSA_FLAG_CAUSAL_ONLY) == 0;
   return indexer_rows(p, s, q_I, k_I, w, row_begin, rows, scores, p->S_k, fill, c,
                       (cudaStream_t)stream);
+}
+
+int dsa_indexer_topk(const dsa_params* p, const void* q_I, const void* k_I, const void* w,
+                     int64_t row_begin, int64_t rows, int32_t* idx, void* workspace,
+                     dsa_stream_t stream) {
+  Shape s;
+  int rc = check_params(p, &s);
+  if (rc) return rc;
+  if (!fused_topk_shape(p)) return DSA_ERR_UNSUPPORTED;
+  if (!q_I || !k_I || !w || !idx) return DSA_ERR_INVALID_ARG;
+  if (row_begin < 0 || rows < 1 || row_begin + rows > p->B * p->S_q) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_I) || !aligned16(k_I)) return DSA_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return DSA_ERR_WORKSPACE;
+  DevCtx c;
+  if (!dev_ctx(&c)) return DSA_ERR_CUDA;
+  return indexer_topk_waves(p, s, q_I, k_I, w, row_begin, rows, idx, workspace, c,
+                            (cudaStream_t)stream);
 }
 
 int dsa_indexer_quantize_fp8(const dsa_params* p, const void* q_I, const void* k_I, uint8_t* q8,
@@ -492,6 +548,12 @@ int dsa_forward(const dsa_params* p, const void* q_I, const void* k_I, const voi
   if (!dev_ctx(&c)) return DSA_ERR_CUDA;
   cudaStream_t st = (cudaStream_t)stream;
   const long long total = p->B * p->S_q, W = wave_rows(p);
+  if (p->flags & DSA_FLAG_FUSED_TOPK) {
+    if (!fused_topk_shape(p)) return DSA_ERR_UNSUPPORTED;
+    rc = indexer_topk_waves(p, s, q_I, k_I, w, 0, total, idx_out, workspace, c, st);
+    if (rc) return rc;
+    return attn_fwd(p, s, q, kv, idx_out, out, softmax_max, softmax_sum, c, st);
+  }
   float* ring = (float*)workspace;
   const bool fp8 = (p->flags & DSA_FLAG_FP8_INDEXER) != 0;
   uint8_t *q8 = nullptr, *k8 = nullptr;

@@ -15,6 +15,19 @@
 //
 // Warp roles: warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer,
 // warps 2..9 = epilogue (two warps per TMEM lane quadrant, two tokens each).
+//
+// Fused form (kFused): the scores never leave the SM.  Each token keeps a
+// running threshold T in shared memory; after every key block the epilogue
+// appends the block's keys whose order-preserving key is >= T to the row's
+// candidate list in global memory (value key and position; one warp-wide
+// compaction per token and block) and counts them in a 2048-bin histogram of
+// the key's upper 11 bits.  T is then raised to the lower edge of the highest
+// bin b with (candidates in bins >= b) >= k: at least k candidates are >= T,
+// so T never exceeds the row's k-th largest key, every key that can be in
+// the top k is kept, and the exact selection runs over the candidates alone
+// (topk.cu).  Every candidate admitted while T stood is in a bin >= b, so a
+// running count of the candidates in bins >= b is exact.  The four warps of
+// a token pair meet at two named barriers per block around the update.
 #include <math.h>
 
 #include "dsa_common.cuh"
@@ -36,22 +49,33 @@ constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr int kTmemCols = 512;
 constexpr uint32_t kIdesc = idesc_bf16(128, kN, false, false);
 
+constexpr int kCandBins = 2048;           // histogram of the key's upper 11 bits
+
 struct __align__(1024) Smem {
   uint8_t a[kStages][kAStage];
   uint8_t b[kBBytes];
   float w[kTQ][kHI];
   long long pos[kTQ];
+  // fused form: per token, bin counts (two 16-bit counts per word), the
+  // threshold, the candidates so far, those already counted, the count in
+  // bins >= bstar, and the group's abort vote
+  uint32_t hist[kTQ][kCandBins / 2];
+  uint32_t thr[kTQ], cnt[kTQ], seen[kTQ], cum[kTQ], bstar[kTQ];
+  int grp_fail[2];
   uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2], b_full, mma_done;
   uint32_t tmem_base;
   int abort;
   int nkb;
 };
+static_assert(sizeof(Smem) + 1024 <= 232448, "indexer shared memory");
 
+template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       Shape s, const __nv_bfloat16* __restrict__ w, long long row_lo,
                       long long row_hi, long long row_begin, int batch,
-                      float* __restrict__ scores, long long ld, DevCtx c) {
+                      float* __restrict__ scores, long long ld, uint32_t* __restrict__ cand_key,
+                      int32_t* __restrict__ cand_pos, uint32_t* __restrict__ cand_cnt, DevCtx c) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -87,8 +111,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       maxpos = p > maxpos ? p : maxpos;
     }
     sm.nkb = (int)((maxpos + kBK) / kBK);  // 0 when no row is valid
+    for (int j = 0; j < kTQ; ++j) sm.thr[j] = sm.cnt[j] = sm.seen[j] = sm.cum[j] = sm.bstar[j] = 0;
+    sm.grp_fail[0] = sm.grp_fail[1] = 0;
     fence_mbar_init();
   }
+  if (kFused)
+    for (int i = threadIdx.x; i < kTQ * kCandBins / 2; i += kThreads) (&sm.hist[0][0])[i] = 0;
   if (threadIdx.x >= 64) {
     const int e = threadIdx.x - 64;  // 256 epilogue threads load w for the 4 rows
     const int j = e / kHI, h = e % kHI;
@@ -162,16 +190,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 2;
     const int quad = warp & 3;       // TMEM lanes this warp may access
     const int half = ew >> 2;        // tokens {2*half, 2*half+1}
+    const int k = s.topk;
     for (int kb = 0; kb < nkb; ++kb) {
       const int acc = kb & 1;
-      if (!mbar_wait_warp(smem_u32(&sm.acc_full[acc]), (kb >> 1) & 1, c, abort_flag)) break;
+      const bool ok_w = mbar_wait_warp(smem_u32(&sm.acc_full[acc]), (kb >> 1) & 1, c, abort_flag);
+      if (!kFused && !ok_w) break;
+      if (kFused && !ok_w && lane == 0) sm.grp_fail[half] = 1;
       tc_fence_after();
       const long long key = (long long)kb * kBK + quad * 32 + lane;
 #pragma unroll
       for (int tt = 0; tt < 2; ++tt) {
         const int j = half * 2 + tt;
         const long long p = sm.pos[j];
-        if (p < (long long)kb * kBK) continue;  // whole block masked for this row (warp-uniform)
+        if (!ok_w || p < (long long)kb * kBK) continue;  // whole block masked for this row (warp-uniform)
         const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + acc * kN + j * kHI;
         uint32_t v0[32], v1[32];
         tmem_ld32(ta, v0);
@@ -196,10 +227,63 @@ __global__ void __launch_bounds__(kThreads, 1)
           a2 = fmaf(wa.z, fmaxf(__uint_as_float(v1[h + 2]), 0.f), a2);
           a3 = fmaf(wa.w, fmaxf(__uint_as_float(v1[h + 3]), 0.f), a3);
         }
-        if (key <= p) scores[(r0 + j - row_begin) * ld + key] = (a0 + a1) + (a2 + a3);
+        const float score = (a0 + a1) + (a2 + a3);
+        if (!kFused) {
+          if (key <= p) scores[(r0 + j - row_begin) * ld + key] = score;
+        } else if (p >= k) {  // rows with at most k visible keys take all of them: no list
+          const uint32_t u = ordered_key(score);
+          const bool is_c = key <= p && u >= sm.thr[j];
+          const uint32_t bal = __ballot_sync(0xffffffffu, is_c);
+          if (bal) {
+            uint32_t base = 0;
+            if (lane == 0) base = atomicAdd(&sm.cnt[j], (uint32_t)__popc(bal));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (is_c) {
+              const long long at = (r0 + j - row_begin) * ld + base + __popc(bal & ((1u << lane) - 1u));
+              cand_key[at] = u;
+              cand_pos[at] = (int32_t)key;
+              atomicAdd(&sm.hist[j][u >> 22], 1u << (16 * ((u >> 21) & 1u)));
+            }
+          }
+        }
+      }
+      if (kFused) {
+        // the group's candidates of this block are counted; one thread
+        // raises the two tokens' thresholds while the group waits
+        named_bar_sync(2 + half, 128);
+        const bool fail = sm.grp_fail[half] != 0;
+        if (!fail && quad == 0 && lane == 0) {
+#pragma unroll 1
+          for (int tt = 0; tt < 2; ++tt) {
+            const int j = half * 2 + tt;
+            if (sm.pos[j] < k) continue;
+            const uint32_t total = sm.cnt[j];
+            uint32_t cum = sm.cum[j] + (total - sm.seen[j]);
+            uint32_t b = sm.bstar[j];
+            while (b + 1 < (uint32_t)kCandBins) {
+              const uint32_t hb = (sm.hist[j][b >> 1] >> (16 * (b & 1u))) & 0xFFFFu;
+              if (cum - hb < (uint32_t)k) break;
+              cum -= hb;
+              ++b;
+            }
+            sm.seen[j] = total;
+            sm.cum[j] = cum;
+            sm.bstar[j] = b;
+            sm.thr[j] = b << 21;
+          }
+        }
+        named_bar_sync(2 + half, 128);
+        if (fail) break;
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.acc_empty[acc]));
+    }
+    if (kFused) {
+      named_bar_sync(2 + half, 128);  // the group's last candidates are counted
+      if (quad == 0 && lane < 2) {
+        const int j = half * 2 + lane;
+        if (r0 + j < row_hi) cand_cnt[r0 + j - row_begin] = sm.pos[j] >= k ? sm.cnt[j] : 0u;
+      }
     }
   }
   __syncthreads();
@@ -215,16 +299,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 bool make_tmap_2d_bf16(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
                        uint32_t box_cols, uint32_t box_rows, int swizzle_bytes);
 
-int launch_indexer_tc(const Shape& s, const void* q_I, const void* k_I, const void* w,
-                      long long row_begin, long long rows, float* scores, long long ld, DevCtx c,
-                      cudaStream_t st) {
-  using namespace idxtc;
+namespace idxtc {
+template <bool kFused>
+static int launch(const Shape& s, const void* q_I, const void* k_I, const void* w, long long row_begin,
+                  long long rows, float* scores, long long ld, uint32_t* cand_key,
+                  int32_t* cand_pos, uint32_t* cand_cnt, DevCtx c, cudaStream_t st) {
   CUtensorMap tq, tk;
   if (!make_tmap_2d_bf16(&tq, q_I, (uint64_t)s.B * s.S_q * kHI, kDI, 64, kN, 128)) return DSA_ERR_CUDA;
   if (!make_tmap_2d_bf16(&tk, k_I, (uint64_t)s.B * s.S_k, kDI, 64, kBK, 128)) return DSA_ERR_CUDA;
   const size_t smem = sizeof(Smem) + 1024;
   // per call: the attribute belongs to the current device's context
-  if (cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(indexer_tc_kernel<kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return DSA_ERR_CUDA;
   const long long r_end = row_begin + rows;
@@ -233,11 +318,33 @@ int launch_indexer_tc(const Shape& s, const void* q_I, const void* k_I, const vo
     const long long hi = r_end < (long long)(b + 1) * s.S_q ? r_end : (long long)(b + 1) * s.S_q;
     if (hi <= lo) continue;
     const long long ntiles = (hi - lo + kTQ - 1) / kTQ;
-    indexer_tc_kernel<<<(unsigned)ntiles, kThreads, smem, st>>>(
-        tq, tk, s, (const __nv_bfloat16*)w, lo, hi, row_begin, b, scores, ld, c);
+    indexer_tc_kernel<kFused><<<(unsigned)ntiles, kThreads, smem, st>>>(
+        tq, tk, s, (const __nv_bfloat16*)w, lo, hi, row_begin, b, scores, ld, cand_key, cand_pos,
+        cand_cnt, c);
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
   }
   return DSA_OK;
+}
+}  // namespace idxtc
+
+int launch_indexer_tc(const Shape& s, const void* q_I, const void* k_I, const void* w,
+                      long long row_begin, long long rows, float* scores, long long ld, DevCtx c,
+                      cudaStream_t st) {
+  return idxtc::launch<false>(s, q_I, k_I, w, row_begin, rows, scores, ld, nullptr, nullptr, nullptr,
+                              c, st);
+}
+
+// Fused indexer + candidate filter: for rows [row_begin, row_begin + rows),
+// row r's candidates (order-preserving keys, positions) go to
+// cand_key / cand_pos [(r - row_begin) * ld ...] and their number to
+// cand_cnt[r - row_begin] (0 for rows with at most k visible keys).
+// ld >= S_k; S_k < 65536 (16-bit bin counts).
+int launch_indexer_topk_tc(const Shape& s, const void* q_I, const void* k_I, const void* w,
+                           long long row_begin, long long rows, uint32_t* cand_key, int32_t* cand_pos,
+                           uint32_t* cand_cnt, long long ld, DevCtx c, cudaStream_t st) {
+  if (s.S_k >= 65536 || ld < s.S_k) return DSA_ERR_UNSUPPORTED;
+  return idxtc::launch<true>(s, q_I, k_I, w, row_begin, rows, nullptr, ld, cand_key, cand_pos, cand_cnt,
+                             c, st);
 }
 
 }  // namespace dsa

@@ -57,7 +57,7 @@ extern "C" int dsa_forward_static_ws(const dsa_params* p, const void* q_I, const
   if (rc) return rc;
   if (!q_I || !k_I || !w || !q || !kv || !idx_out || !out || !softmax_max || !softmax_sum)
     return DSA_ERR_INVALID_ARG;
-  if (p->flags & DSA_FLAG_FP8_INDEXER) return DSA_ERR_UNSUPPORTED;  // bf16 indexer only
+  if (p->flags & (DSA_FLAG_FP8_INDEXER | DSA_FLAG_FUSED_TOPK)) return DSA_ERR_UNSUPPORTED;  // the ring path only
   rc = ext_attn_fwd_supported(p, s, q, kv, out);
   if (rc) return rc;
   if (p->dtype == DSA_BF16 &&

@@ -511,6 +511,99 @@ __global__ void __launch_bounds__(TK_THREADS, 1)
   }
 }
 
+// Exact top-k over the candidates the fused indexer kept for each row
+// (indexer_tc.cu, kFused): every key that can be among the row's k largest is
+// a candidate, so the radix select over the candidates' keys finds the row's
+// threshold.  Candidates arrive in no particular order; they are marked in
+// two position bitmaps (above the threshold / equal to it) and one scan over
+// the bitmaps in position order writes the winners sorted, the lowest
+// positions among equal keys first.  One CTA per row.
+__global__ void __launch_bounds__(TK_THREADS, 1)
+    topk_cand_kernel(Shape s, const uint32_t* __restrict__ cand_key,
+                     const int32_t* __restrict__ cand_pos, const uint32_t* __restrict__ cand_cnt,
+                     long long ld, long long row_begin, int32_t* __restrict__ idx, DevCtx c) {
+  __shared__ TopkSmem sm;
+  extern __shared__ uint32_t marks[];  // [nw] above the threshold | [nw] equal to it
+  const long long r_local = blockIdx.x;
+  const long long row = row_begin + r_local;
+  const int k = s.topk;
+  int32_t* out = idx + r_local * (long long)k;
+  const long long pos = row_pos(s, row);
+  if (pos < 0 || pos >= s.S_k) {
+    if (threadIdx.x == 0) set_status(c, DSA_ERR_INDEX);
+    write_prefix_rows(out, 0, k);
+    return;
+  }
+  const int n = (int)pos + 1;
+  if (n <= k) {
+    write_prefix_rows(out, n, k);
+    return;
+  }
+  const uint32_t m = cand_cnt[r_local] < (uint32_t)n ? cand_cnt[r_local] : (uint32_t)n;
+  const uint32_t* ck = cand_key + r_local * ld;
+  const int32_t* cp = cand_pos + r_local * ld;
+  auto for_each = [&](auto fn) {
+    for (uint32_t i = threadIdx.x; i < m; i += TK_THREADS) fn(ck[i]);
+  };
+  int sh;
+  uint32_t tp, take_eq;
+  radix_select(sm, k, for_each, sh, tp, take_eq);
+  const int nw = (n + 31) >> 5;
+  uint32_t* gtb = marks;
+  uint32_t* eqb = marks + nw;
+  for (int i = threadIdx.x; i < 2 * nw; i += TK_THREADS) marks[i] = 0;
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i < m; i += TK_THREADS) {
+    const uint32_t kk = ck[i] >> sh;
+    const int p = cp[i];
+    if (p < 0 || p >= n) continue;
+    if (kk > tp)
+      atomicOr(&gtb[p >> 5], 1u << (p & 31));
+    else if (kk == tp)
+      atomicOr(&eqb[p >> 5], 1u << (p & 31));
+  }
+  __syncthreads();
+  // thread t scans the words [t * wpt, t * wpt + wpt), in position order
+  const int wpt = (nw + TK_THREADS - 1) / TK_THREADS;
+  const int w0 = threadIdx.x * wpt;
+  unsigned long long cnt = 0;
+  for (int i = 0; i < wpt; ++i)
+    if (w0 + i < nw)
+      cnt += (unsigned long long)__popc(gtb[w0 + i]) | ((unsigned long long)__popc(eqb[w0 + i]) << 32);
+  unsigned long long total;
+  const unsigned long long pre = block_scan_excl<unsigned long long>(cnt, sm.warp_sum64, &sm.total64, total);
+  uint32_t gt_b = (uint32_t)(pre & 0xFFFFFFFFull), eq_b = (uint32_t)(pre >> 32);
+  for (int i = 0; i < wpt && w0 + i < nw; ++i) {
+    const uint32_t g = gtb[w0 + i], e = eqb[w0 + i];
+    for (uint32_t mm = g | e; mm; mm &= mm - 1u) {
+      const int b = __ffs(mm) - 1;
+      const int q = (w0 + i) * 32 + b;
+      if ((g >> b) & 1u) {
+        const uint32_t o = gt_b + min(eq_b, take_eq);
+        if (o < (uint32_t)k) out[o] = q;
+        ++gt_b;
+      } else {
+        if (eq_b < take_eq && gt_b + eq_b < (uint32_t)k) out[gt_b + eq_b] = q;
+        ++eq_b;
+      }
+    }
+  }
+}
+
+int launch_topk_cand(const Shape& s, const uint32_t* cand_key, const int32_t* cand_pos,
+                     const uint32_t* cand_cnt, long long ld, long long row_begin, long long rows,
+                     int32_t* idx, DevCtx c, cudaStream_t st) {
+  if (rows <= 0) return DSA_OK;
+  const size_t marks = 2 * (size_t)((s.S_k + 31) / 32) * sizeof(uint32_t);
+  if (marks > 48 * 1024 &&
+      cudaFuncSetAttribute(topk_cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)marks) !=
+          cudaSuccess)
+    return DSA_ERR_CUDA;
+  topk_cand_kernel<<<(unsigned)rows, TK_THREADS, marks, st>>>(s, cand_key, cand_pos, cand_cnt, ld,
+                                                               row_begin, idx, c);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
 bool make_tmap_f32_lines(CUtensorMap* tm, const float* base, uint64_t rows, uint64_t ld,
                          uint64_t lines, uint32_t box_lines);
 
