@@ -136,6 +136,31 @@ def fp8_indexer_stage(dsa, dev, wl, x, waves, steps, peak_tc):
             "note": "E4M3 q_I, k_I with one fp32 scale per 128-vector; outside the timed step"}
 
 
+def fused_topk_stage(dsa, dev, wl, x, idx_ref, steps):
+    """The fused indexer + streaming top-k (dsa_indexer_topk) over the step's
+    rows, outside the timed step, and the whole forward with it
+    (DSA_FLAG_FUSED_TOPK); its indices are checked against the step's."""
+    S, k = wl["S"], wl["topk"]
+    p = dsa.make_params(B=1, S_q=S, S_k=S, H=wl["H"], d_qk=wl["d_qk"], d_v=wl["d_v"], H_I=wl["H_I"],
+                        d_I=wl["d_I"], topk=k, scale=wl["scale"], dtype="bf16",
+                        flags=dsa.DSA_FLAG_FUSED_TOPK)
+    st = torch.cuda.current_stream(dev)
+    ws = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_INDEXER_TOPK), dtype=torch.uint8, device=dev)
+    idx = torch.empty(1, S, k, dtype=torch.int32, device=dev)
+    t_sel = time_calls(lambda: dsa.indexer_topk(p, x["q_I"], x["k_I"], x["w"], 0, S, idx, ws), steps, 2, st)
+    same = bool(torch.equal(idx, idx_ref))
+    out = torch.empty(1, S, wl["H"], wl["d_v"], dtype=torch.bfloat16, device=dev)
+    m = torch.empty(1, S, wl["H"], device=dev)
+    l = torch.empty_like(m)
+    t_fwd = time_calls(lambda: dsa.forward(p, x["q_I"], x["k_I"], x["w"], x["q"], x["kv"], idx, out, m, l,
+                                           ws), steps, 2, st)
+    assert dsa.get_status() == 0
+    return {"indexer_topk_ms": t_sel, "forward_ms": t_fwd, "forward_tokens_per_s": S / (t_fwd * 1e-3),
+            "equals_unfused": same,
+            "note": "indexer + top-k fused (candidate lists instead of the score ring); outside the "
+                    "timed step, no L2 flush between calls"}
+
+
 def backward_stage(dsa, dev, steps, peak_tc, workload="dsv32_S16384_train", rows=None):
     """The training-shape backward (S = 16384, top-2048, all rows): the forward,
     the attention backward (dq, dkv), the indexer KL-loss backward, each timed
@@ -378,7 +403,7 @@ def main():
     ap.add_argument("--no-bwd", action="store_true", help="skip the training-shape backward timing")
     ap.add_argument("--rows", type=int, default=None,
                     help="with --stage bwd: the last N query rows against all keys (profiling)")
-    ap.add_argument("--stage", default=None, choices=["topk", "bwd", "fp8idx"],
+    ap.add_argument("--stage", default=None, choices=["topk", "bwd", "fp8idx", "fused"],
                     help="time one stage alone (a profiling aid; prints its own JSON line)")
     args = ap.parse_args()
     wl = synth.WORKLOADS[args.workload]
@@ -410,6 +435,27 @@ def main():
         wv = [(r0, min(W0, S0 - r0)) for r0 in range(0, S0, W0)]
         r = fp8_indexer_stage(dsa, dev, wl, xi, wv, args.steps, load_peaks()["bf16_tflops"])
         print(json.dumps(dict(stage="fp8idx", workload=wl["name"], **r)), flush=True)
+        return
+    if args.stage == "fused":
+        S0, k0 = wl["S"], wl["topk"]
+        xi = synth.make_inputs(wl, device=dev)
+        p0 = dsa.make_params(B=1, S_q=S0, S_k=S0, H=wl["H"], d_qk=wl["d_qk"], d_v=wl["d_v"], H_I=wl["H_I"],
+                             d_I=wl["d_I"], topk=k0, scale=wl["scale"], dtype="bf16",
+                             flags=dsa.DSA_FLAG_CAUSAL_ONLY)  # as dsa_forward's ring
+        ring0 = torch.empty(dsa.workspace_size(p0, dsa.DSA_CALL_FORWARD), dtype=torch.uint8, device=dev)
+        idx0 = torch.empty(1, S0, k0, dtype=torch.int32, device=dev)
+        W0 = dsa.wave_rows(p0)
+        sc0 = torch.empty(W0, S0, device=dev)
+        def plain():
+            for r0 in range(0, S0, W0):
+                n0 = min(W0, S0 - r0)
+                dsa.indexer_scores(p0, xi["q_I"], xi["k_I"], xi["w"], r0, n0, sc0)
+                dsa.topk(p0, sc0, r0, n0, idx0[0, r0:r0 + n0])
+        t_plain = time_calls(plain, args.steps, 2, torch.cuda.current_stream(dev))
+        del ring0
+        r = fused_topk_stage(dsa, dev, wl, xi, idx0, args.steps)
+        print(json.dumps(dict(stage="fused", workload=wl["name"], indexer_then_topk_ms=t_plain, **r)),
+              flush=True)
         return
     if args.stage == "bwd":
         wname = args.workload if args.workload != "dsv32_S32768" else "dsv32_S16384_train"
@@ -598,9 +644,10 @@ def main():
                "equals_whole_call": same}
         assert dsa.get_status() == 0
 
-    fp8i = None
+    fp8i = fused = None
     if rank == 0:
         fp8i = fp8_indexer_stage(dsa, dev, wl, x, waves, max(2, min(K, 5)), peak_tc)
+        fused = fused_topk_stage(dsa, dev, wl, x, idx, max(2, min(K, 5)))
     bwd = None
     if not args.no_bwd and rank == 0:
         del x, out, ring, idx, m, l, flush
@@ -649,6 +696,7 @@ def main():
         "cpu_baseline": cpu,
         "backward": bwd,
         "fp8_indexer": fp8i,
+        "fused_topk": fused,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -27,7 +27,8 @@
 // the top k is kept, and the exact selection runs over the candidates alone
 // (topk.cu).  Every candidate admitted while T stood is in a bin >= b, so a
 // running count of the candidates in bins >= b is exact.  The four warps of
-// a token pair meet at two named barriers per block around the update.
+// a token pair meet at two named barriers around each update (every 8 key
+// blocks and after the last one).
 #include <math.h>
 
 #include "dsa_common.cuh"
@@ -50,6 +51,16 @@ constexpr int kTmemCols = 512;
 constexpr uint32_t kIdesc = idesc_bf16(128, kN, false, false);
 
 constexpr int kCandBins = 2048;           // histogram of the key's upper 11 bits
+
+__device__ __forceinline__ uint32_t warp_incl_scan_u32(uint32_t x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+constexpr int kUpdateEvery = 8;           // key blocks between threshold updates
 
 struct __align__(1024) Smem {
   uint8_t a[kStages][kAStage];
@@ -195,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int acc = kb & 1;
       const bool ok_w = mbar_wait_warp(smem_u32(&sm.acc_full[acc]), (kb >> 1) & 1, c, abort_flag);
       if (!kFused && !ok_w) break;
-      if (kFused && !ok_w && lane == 0) sm.grp_fail[half] = 1;
+      if (kFused && !ok_w && lane == 0) sm.grp_fail[half] = 1;  // read at the next update
       tc_fence_after();
       const long long key = (long long)kb * kBK + quad * 32 + lane;
 #pragma unroll
@@ -242,17 +253,26 @@ __global__ void __launch_bounds__(kThreads, 1)
               const long long at = (r0 + j - row_begin) * ld + base + __popc(bal & ((1u << lane) - 1u));
               cand_key[at] = u;
               cand_pos[at] = (int32_t)key;
-              atomicAdd(&sm.hist[j][u >> 22], 1u << (16 * ((u >> 21) & 1u)));
+              // one shared atomic per distinct bin of the warp's candidates
+              const uint32_t bin = u >> 21;
+              const uint32_t peers = __match_any_sync(bal, bin);
+              if (lane == __ffs(peers) - 1)
+                atomicAdd(&sm.hist[j][bin >> 1], (uint32_t)__popc(peers) << (16 * (bin & 1u)));
             }
           }
         }
       }
-      if (kFused) {
-        // the group's candidates of this block are counted; one thread
-        // raises the two tokens' thresholds while the group waits
+      if (kFused && ((kb & (kUpdateEvery - 1)) == kUpdateEvery - 1 || kb == nkb - 1)) {
+        // every kUpdateEvery blocks: the group's candidates so far are
+        // counted; one thread raises the two tokens' thresholds while the
+        // group waits (a warp whose wait failed keeps walking the blocks
+        // without work until here, so the group leaves together)
         named_bar_sync(2 + half, 128);
         const bool fail = sm.grp_fail[half] != 0;
-        if (!fail && quad == 0 && lane == 0) {
+        if (!fail && quad == 0) {
+          // one warp advances each token's bin pointer 32 bins at a time:
+          // past bin b while the candidates in the bins above it still
+          // number >= k (cum - prefix >= k, monotone over the lanes)
 #pragma unroll 1
           for (int tt = 0; tt < 2; ++tt) {
             const int j = half * 2 + tt;
@@ -260,16 +280,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t total = sm.cnt[j];
             uint32_t cum = sm.cum[j] + (total - sm.seen[j]);
             uint32_t b = sm.bstar[j];
-            while (b + 1 < (uint32_t)kCandBins) {
-              const uint32_t hb = (sm.hist[j][b >> 1] >> (16 * (b & 1u))) & 0xFFFFu;
-              if (cum - hb < (uint32_t)k) break;
-              cum -= hb;
-              ++b;
+            for (;;) {
+              const uint32_t bb = b + lane;
+              const uint32_t h = bb < (uint32_t)kCandBins ? (sm.hist[j][bb >> 1] >> (16 * (bb & 1u))) & 0xFFFFu : 0u;
+              const uint32_t pre = warp_incl_scan_u32(h, lane);
+              const bool adv_ok = bb + 1 < (uint32_t)kCandBins && cum - pre >= (uint32_t)k;
+              const int adv = __popc(__ballot_sync(0xffffffffu, adv_ok));
+              if (adv > 0) {
+                cum -= __shfl_sync(0xffffffffu, pre, adv - 1);
+                b += adv;
+              }
+              if (adv < 32) break;
             }
-            sm.seen[j] = total;
-            sm.cum[j] = cum;
-            sm.bstar[j] = b;
-            sm.thr[j] = b << 21;
+            if (lane == 0) {
+              sm.seen[j] = total;
+              sm.cum[j] = cum;
+              sm.bstar[j] = b;
+              sm.thr[j] = b << 21;
+            }
           }
         }
         named_bar_sync(2 + half, 128);
