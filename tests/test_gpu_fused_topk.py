@@ -120,3 +120,23 @@ def test_forward_fused_flag_equals_plain():
         res.append((idx, out, m, l))
     for a, b in zip(*res):
         assert torch.equal(a, b)
+
+
+def test_fused_batches_and_head_tail_rows():
+    # B = 2 (rows of both batches in one call, each against its own keys) and
+    # a head-tail context-parallel shard given by q_row_index
+    dsa = lib()
+    S, k = 2048, 256
+    wl = dict(synth.v32(S, "b2"), B=2, topk=k)
+    x = _indexer_inputs(wl, S, seed=3)
+    p = params(dsa, wl, B=2)
+    _assert_equal(*_both(dsa, p, x, 0, 2 * S))
+    _assert_equal(*_both(dsa, p, x, S - 100, 300))       # straddles the batch boundary
+    rows = np.r_[0:256, S - 256:S].astype(np.int32)      # head and tail of one sequence
+    ridx = torch.as_tensor(rows, device=DEV)
+    wl1 = dict(synth.v32(S, "ht"), topk=k)
+    x1 = _indexer_inputs(wl1, S, seed=4)
+    sel = torch.as_tensor(rows, dtype=torch.long, device=DEV)
+    x1 = dict(q_I=x1["q_I"][:, sel].contiguous(), k_I=x1["k_I"], w=x1["w"][:, sel].contiguous())
+    p1 = params(dsa, wl1, S_q=len(rows), q_row_index=ridx)
+    _assert_equal(*_both(dsa, p1, x1, 0, len(rows)))
