@@ -566,11 +566,16 @@ def main():
         # independent, so the results equal one whole-sequence call bit for
         # bit.  Chunks run from the last rows to the first: causal rows get
         # cheaper towards the start while their copies do not, so the heavy
-        # chunks hide the copies of the light ones; the first and last chunks
-        # are small so that the copy-in before the first compute and the
-        # copy-out after the last one are short.
-        if S % 4096 == 0 and S >= 16384:
-            sizes = [1024, 3072] + [4096] * (S // 4096 - 2) + [3072, 1024]
+        # chunks hide the copies of the light ones.  Each chunk but the last
+        # (the lightest) is two indexer waves, so no wave of a chunk runs
+        # with idle SMs.  The device inputs are double-buffered across steps
+        # (a data loader's prefetch): step s copies into buffer s % 2 once
+        # step s - 2's compute has released it, so the next step's copies run
+        # under this step's compute, and the first chunk's copy-in and the
+        # last chunk's copy-out overlap the neighbouring steps.
+        c_rows = 2 * dsa.wave_rows(p)
+        if S >= 4 * c_rows:
+            sizes = [c_rows] * (S // c_rows) + ([S % c_rows] if S % c_rows else [])
         else:
             sizes = [S]
         bounds = []
@@ -586,28 +591,31 @@ def main():
             pr.S_q = r1 - r0
             pc.append(pr)
         rows = lambda t, c: t[:, bounds[c][0]:bounds[c][1]]
-        prev = {"cmp": None, "out": [None] * nch}
+        xs = (x, {n: torch.empty_like(v) for n, v in x.items()})
+        prev = {"cmp": [None, None], "out": [None] * nch, "step": 0}
 
         def e2e_step():
             e_kv, e_in, e_done, e_out = E(), [E() for _ in range(nch)], [E() for _ in range(nch)], \
                 [E() for _ in range(nch)]
+            buf = prev["step"] % 2
+            xb = xs[buf]
             with torch.cuda.stream(s_in):
-                if prev["cmp"] is not None:     # the previous step no longer reads the inputs
-                    s_in.wait_event(prev["cmp"])
-                x["k_I"].copy_(host_in["k_I"], non_blocking=True)
-                x["kv"].copy_(host_in["kv"], non_blocking=True)
+                if prev["cmp"][buf] is not None:  # step - 2 no longer reads this input buffer
+                    s_in.wait_event(prev["cmp"][buf])
+                xb["k_I"].copy_(host_in["k_I"], non_blocking=True)
+                xb["kv"].copy_(host_in["kv"], non_blocking=True)
                 e_kv.record(s_in)
                 for c in range(nch):
                     for n in ("q_I", "w", "q"):
-                        rows(x[n], c).copy_(rows(host_in[n], c), non_blocking=True)
+                        rows(xb[n], c).copy_(rows(host_in[n], c), non_blocking=True)
                     e_in[c].record(s_in)
             s_cmp.wait_event(e_kv)
             for c in range(nch):
                 s_cmp.wait_event(e_in[c])
                 if prev["out"][c] is not None:  # the previous step's outputs are copied out
                     s_cmp.wait_event(prev["out"][c])
-                dsa.forward(pc[c], rows(x["q_I"], c), x["k_I"], rows(x["w"], c), rows(x["q"], c),
-                            x["kv"], rows(idx, c), rows(out, c), rows(m, c), rows(l, c), ring,
+                dsa.forward(pc[c], rows(xb["q_I"], c), xb["k_I"], rows(xb["w"], c), rows(xb["q"], c),
+                            xb["kv"], rows(idx, c), rows(out, c), rows(m, c), rows(l, c), ring,
                             stream=s_cmp)
                 e_done[c].record(s_cmp)
             with torch.cuda.stream(s_out):
@@ -616,7 +624,8 @@ def main():
                     for n, t in (("idx", idx), ("out", out), ("m", m), ("l", l)):
                         rows(host_out[n], c).copy_(rows(t, c), non_blocking=True)
                     e_out[c].record(s_out)
-            prev["cmp"], prev["out"] = e_done[-1], e_out
+            prev["cmp"][buf], prev["out"] = e_done[-1], e_out
+            prev["step"] += 1
             return e_out[-1]
 
         for _ in range(2):
@@ -639,6 +648,7 @@ def main():
                     ref["m"], ref["l"], ring)
         torch.cuda.synchronize()
         same = all(torch.equal(ref[n].cpu(), host_out[n]) for n in ref)
+        del xs, ref  # the second input buffer
         e2e = {"value": job_value(world, S, ms_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "row_chunks": nch,
                "equals_whole_call": same}
