@@ -54,8 +54,10 @@
 // the relay thread (a proxy fence, then a cluster-scope arrive).
 //
 // Roles per CTA: warp 0 = TMEM allocation, the MMA issuer in CTA 0 and the
-// relay in CTA 1; warps 1..4 = kv gather; warps 5..12 = query columns
-// into TMEM, softmax and epilogue (warp w: TMEM lane quadrant w % 4, logit
+// relay in CTA 1; warps 1..4 = kv gather and each token's query columns into
+// TMEM (as soon as the previous token's last logits MMA is done, so the
+// softmax warps go straight from a token's last block to its epilogue);
+// warps 5..12 = softmax and epilogue (warp w: TMEM lane quadrant w % 4, logit
 // columns [56ch, 56ch+56) with ch = (w - 5) / 4); warp 13 = index scan of
 // the coming tokens (valid-slot masks, block count, out-of-range report) and
 // an L2 prefetch of their query rows.
@@ -100,9 +102,10 @@ struct __align__(1024) Smem {
   int nblk[2];                                     // per token: blocks up to the last valid slot
   float red[kSoftWarps][32];                       // per-warp partial block maxima / row sums
   uint32_t sink[kSoftWarps];                       // targets of CTA 1's signalling stores
+  uint32_t sink_g[kGatherWarps];                   // (those of its gather warps)
   uint64_t st_full[kStages], st_empty[kStages];
   uint64_t s_full, s_free, p_full[2];
-  uint64_t q_tm[2], mma_done[2], sc_full[2], sc_empty[2], fin;
+  uint64_t q_tm[2], q_free[2], mma_done[2], sc_full[2], sc_empty[2], fin;
   uint32_t tmem_base;
   int abort;
 };
@@ -270,7 +273,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&sm.s_free), kSoftWarps);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sm.p_full[i]), kSoftWarps);  // blocks of parity i
-      mbar_init(smem_u32(&sm.q_tm[i]), kSoftWarps);    // tokens of parity i
+      // tokens of parity i: the local gather warps store the query, the first
+      // also expecting CTA 1's gather warps' 4 x 4 bytes (used in CTA 0)
+      mbar_init(smem_u32(&sm.q_tm[i]), kGatherWarps);
+      mbar_init(smem_u32(&sm.q_free[i]), 1);         // the token's last logits MMA done
       mbar_init(smem_u32(&sm.mma_done[i]), 1);
       mbar_init(smem_u32(&sm.sc_full[i]), 1);
       // the gather warps, the softmax warps and the issuer (CTA 0) / relay (CTA 1)
@@ -344,6 +350,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int rcol = kDV + 32 * (int)crank + 8 * rp;
     int G = 0;                                                 // blocks so far (all tokens)
     bool ok = true;
+    // Token i's query columns of this CTA into TMEM (thread = TMEM lane of
+    // this warp's quadrant: head l & 63, lane half l >> 6; value runs ch 0
+    // and 1, rope with ch 0), once the previous token's last logits MMA has
+    // read the old ones; then one arrive per warp on CTA 0's q_tm (CTA 1's
+    // warps: a 4-byte store that completes on it).  Issued after the token's
+    // first block of gathers, so both loads are in flight together.
+    auto store_q = [&](int i) -> bool {
+      if (i > 0) {
+        if (!mbar_wait_warp(smem_u32(&sm.q_free[(i - 1) & 1]), ((i - 1) >> 1) & 1, c, abort_flag))
+          return false;
+        tc_fence_after();
+      }
+      const int l = (warp & 3) * 32 + lane;
+      const long long qrow = nrows - 1 - (pair + (long long)i * npairs);
+      const __nv_bfloat16* qh = q_head(qb, qrow, crank, l & 63);
+      const uint32_t lane_tmem = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+      // 64 value columns at a time (run ch = p >> 1, its half p & 1 -> TMEM
+      // columns kColQ + 32p), then the 32 rope columns -> kColQ + 128
+      const uint4* vsrc = reinterpret_cast<const uint4*>(qh + 128 * (l >> 6));
+#pragma unroll 1
+      for (int p = 0; p < 4; ++p) {
+        uint32_t w[32];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const uint4 a = __ldg(vsrc + 32 * (p >> 1) + 8 * (p & 1) + t);
+          w[4 * t] = a.x, w[4 * t + 1] = a.y, w[4 * t + 2] = a.z, w[4 * t + 3] = a.w;
+        }
+        tmem_st32(lane_tmem + kColQ + 32 * p, w);
+        tmem_st_wait();  // w is reused by the next piece
+      }
+      {
+        const uint4* rsrc = reinterpret_cast<const uint4*>(qh + kDV + 32 * (l >> 6));
+        uint32_t w2[16];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const uint4 a = __ldg(rsrc + t);
+          w2[4 * t] = a.x, w2[4 * t + 1] = a.y, w2[4 * t + 2] = a.z, w2[4 * t + 3] = a.w;
+        }
+        tmem_st16(lane_tmem + kColQ + 128, w2);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t bar = smem_u32(&sm.q_tm[i & 1]);
+        if (crank == 0) {
+          if (gw == 0) mbar_arrive_expect_tx(bar, 4 * kGatherWarps);
+          else mbar_arrive(bar);
+        } else {
+          st_async_signal(mapa_shared(smem_u32(&sm.sink_g[gw]), 0), mapa_shared(bar, 0));
+        }
+      }
+      return true;
+    };
     for (int i = 0; i < ntok && ok; ++i) {
       const int bi = i & 1;
       if (!mbar_wait_warp(smem_u32(&sm.sc_full[bi]), (i >> 1) & 1, c, abort_flag)) break;
@@ -382,7 +442,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                           kvb + (long long)rid * kDQK + rcol);
         }
         cp_async_arrive_noinc(smem_u32(&sm.st_full[st]));
+        if (j == 0 && !store_q(i)) {
+          ok = false;
+          break;
+        }
       }
+      if (ok && nblk == 0 && !store_q(i)) ok = false;  // a token with no block still needs its query
     }
     cp_async_wait_all();  // no copy may still be in flight when the CTA exits
   } else if (warp == 0) {
@@ -428,6 +493,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             commit2(smem_u32(&sm.s_full));
             ++js;
             ++Gs;
+            // the token's query columns are free once its last logits are done
+            if (js == nblk) commit2(smem_u32(&sm.q_free[bi]));
             progressed = true;
           } else if (jp < js && mbar_poll(smem_u32(&sm.p_full[Gp & 1]), (Gp >> 1) & 1)) {
             tc_fence_after();
@@ -458,6 +525,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ok = false;
             }
           }
+        }
+        if (ok && nblk == 0) {  // no logits MMA read this query: free it in both CTAs
+          mbar_arrive(smem_u32(&sm.q_free[bi]));
+          mbar_arrive_remote(mapa_shared(smem_u32(&sm.q_free[bi]), 1));
         }
         commit2(smem_u32(&sm.mma_done[bi]));  // this token's O complete
       }
@@ -529,24 +600,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     };
-    // Query columns of head hl for lane half `half`: run ch of E_half (128
-    // contiguous columns) -> TMEM columns kColQ + 64ch .. +64, and (ch 0) the
-    // rope columns R_half -> kColQ + 128 .. +16 (q_fetch_value: the value
-    // columns into registers; q_store: into TMEM with the rope columns, then
-    // the signal on q_tm[bi]).
     // The 8 softmax warps synchronise with each other through named barriers
     // 1 (bar.sync, 256 threads) and 2 (the per-token vote): every warp
     // executes the same sequence of barriers whatever happens (after a failed
     // wait it keeps going through the token without work, and the vote at the
     // next token makes all of them stop), so they cannot deadlock.
     bool ok = true;
-    if (ntok > 0) {
-      uint32_t w0[32], w1[32];
-      const __nv_bfloat16* qh = q_head(qb, nrows - 1 - pair, crank, hl);
-      q_fetch_value(qh, ch, half, w0, w1);
-      q_store(tmem + lane_off, qh, ch, half, w0, w1);
-      signal(&sm.q_tm[0]);
-    }
     // the epilogue stages O through the P buffers; one thread stores them
     // with TMA and waits for those reads before the buffers are reused
     const bool o_storer = warp == kWarpSoft0 && lane == 0;
@@ -728,18 +787,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // this token's masks are no longer read
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.sc_empty[bi]));
-      // the next token's query into TMEM (this token's last logits have been
-      // read, so its columns are free) before the epilogue, so that the
-      // next token's first logits run during the epilogue (holding the
-      // query in registers across the epilogue spills)
-      const bool next_q = ok && i + 1 < ntok;
-      if (next_q) {
-        uint32_t w0[32], w1[32];
-        const __nv_bfloat16* qh = q_head(qb, row - npairs, crank, hl);
-        q_fetch_value(qh, ch, half, w0, w1);
-        q_store(tmem + lane_off, qh, ch, half, w0, w1);
-        signal(&sm.q_tm[(i + 1) & 1]);
-      }
       // ------------------------------- epilogue -------------------------------
       bool have = ok;
       if (have) have = mbar_wait_warp(smem_u32(&sm.mma_done[bi]), (i >> 1) & 1, c, abort_flag);
