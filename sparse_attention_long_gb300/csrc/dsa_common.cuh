@@ -364,6 +364,39 @@ __device__ __forceinline__ void warp_scatter_add_32x32(uint32_t scratch, const u
   __syncwarp();
 }
 
+// (w0, w1) * (x0, x1) + acc as one packed fp32x2 FMA (each lane rounds like
+// fmaf); acc holds two floats, the first in the low half
+__device__ __forceinline__ uint64_t ffma2(float w0, float w1, float x0, float x1, uint64_t acc) {
+  uint64_t w, x, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(w) : "f"(w0), "f"(w1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(w), "l"(x), "l"(acc));
+  return d;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// Lightning Indexer head reduction of one score: sum_j w[j] * max(x_j, 0)
+// over 64 heads, x_j = v0[j] (j < 32) or v1[j - 32] as fp32 bits, w in
+// shared memory (16-byte aligned).  Four running sums (heads j mod 4),
+// advanced two at a time by packed FMAs, then (s0 + s1) + (s2 + s3).
+__device__ __forceinline__ float relu_wsum64(const uint32_t (&v0)[32], const uint32_t (&v1)[32],
+                                             const float* w) {
+  uint64_t a01 = 0, a23 = 0;  // two +0.0f each
+#pragma unroll
+  for (int h = 0; h < 64; h += 4) {
+    const uint32_t* v = h < 32 ? v0 + h : v1 + (h - 32);
+    const float4 wa = *reinterpret_cast<const float4*>(w + h);
+    a01 = ffma2(wa.x, wa.y, fmaxf(__uint_as_float(v[0]), 0.f), fmaxf(__uint_as_float(v[1]), 0.f), a01);
+    a23 = ffma2(wa.z, wa.w, fmaxf(__uint_as_float(v[2]), 0.f), fmaxf(__uint_as_float(v[3]), 0.f), a23);
+  }
+  float a0, a1, a2, a3;
+  unpack2(a01, a0, a1);
+  unpack2(a23, a2, a3);
+  return (a0 + a1) + (a2 + a3);
+}
+
 // Shared-memory matrix descriptor (tcgen05): start, leading / stride byte
 // offsets, fixed version 1, swizzle layout (0 none, 2 = 128B, 4 = 64B, 6 = 32B).
 constexpr uint32_t kSw128 = 2, kSw64 = 4;

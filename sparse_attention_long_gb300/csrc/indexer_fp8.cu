@@ -192,25 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(ta + 32, v1);
         tmem_ld_wait(v0);
         tmem_ld_also(v1);
-        const float* wj = sm.w[j];
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-        for (int h = 0; h < 32; h += 4) {
-          const float4 wa = *reinterpret_cast<const float4*>(wj + h);
-          a0 = fmaf(wa.x, fmaxf(__uint_as_float(v0[h + 0]), 0.f), a0);
-          a1 = fmaf(wa.y, fmaxf(__uint_as_float(v0[h + 1]), 0.f), a1);
-          a2 = fmaf(wa.z, fmaxf(__uint_as_float(v0[h + 2]), 0.f), a2);
-          a3 = fmaf(wa.w, fmaxf(__uint_as_float(v0[h + 3]), 0.f), a3);
-        }
-#pragma unroll
-        for (int h = 0; h < 32; h += 4) {
-          const float4 wa = *reinterpret_cast<const float4*>(wj + 32 + h);
-          a0 = fmaf(wa.x, fmaxf(__uint_as_float(v1[h + 0]), 0.f), a0);
-          a1 = fmaf(wa.y, fmaxf(__uint_as_float(v1[h + 1]), 0.f), a1);
-          a2 = fmaf(wa.z, fmaxf(__uint_as_float(v1[h + 2]), 0.f), a2);
-          a3 = fmaf(wa.w, fmaxf(__uint_as_float(v1[h + 3]), 0.f), a3);
-        }
-        if (key <= p) scores[(r0 + j - row_begin) * ld + key] = skey * ((a0 + a1) + (a2 + a3));
+        if (key <= p) scores[(r0 + j - row_begin) * ld + key] = skey * relu_wsum64(v0, v1, sm.w[j]);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.acc_empty[acc]));
