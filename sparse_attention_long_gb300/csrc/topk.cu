@@ -93,8 +93,8 @@ __device__ __forceinline__ void find_bin(TopkSmem& sm, int nbins, uint32_t k_rem
   __syncthreads();
 }
 
-__device__ __forceinline__ void write_prefix_rows(int32_t* out, int n, int k) {
-  for (int j = threadIdx.x; j < k; j += TK_THREADS) out[j] = j < n ? j : -1;
+__device__ __forceinline__ void write_prefix_rows(int32_t* out, int n, int k, int nt = TK_THREADS) {
+  for (int j = threadIdx.x; j < k; j += nt) out[j] = j < n ? j : -1;
 }
 
 // Radix passes shared by both variants.  KEYS(fn) must call fn(key) for every
@@ -156,55 +156,55 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x, int lane) {
   return x;
 }
 
-// Exclusive scan of v over the block in thread order; one barrier.  ws must
-// not be written again before the next barrier every thread passes.
+// Exclusive scan of v over the NT threads of the block in thread order; one
+// barrier.  ws must not be written again before the next barrier every
+// thread passes.
+template <int NT>
 __device__ __forceinline__ uint32_t block_excl_scan_1b(uint32_t v, uint32_t* ws) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t x = warp_incl_scan(v, lane);
   if (lane == 31) ws[warp] = x;
   __syncthreads();
-  const uint32_t t = ws[lane];
+  const uint32_t t = lane < NT / 32 ? ws[lane] : 0u;
   const uint32_t ti = warp_incl_scan(t, lane);
   return __shfl_sync(0xffffffffu, ti - t, warp) + x - v;
 }
 
 // The bin b of hist[0..NB), counted from the top, with
 // count(> b) < k_rem <= count(>= b); result in sm.bin / above / bin_count.
-template <int NB>
+template <int NB, int NT>
 __device__ __forceinline__ void find_bin_2b(TopkRegSmem& sm, const uint32_t* hist, uint32_t k_rem) {
-  constexpr int PER = NB >= TK_THREADS ? NB / TK_THREADS : 1;
-  static_assert(PER == 1 || PER == 4, "bins per thread");
+  constexpr int PER = NB >= NT ? NB / NT : 1;
+  static_assert(PER == 1 || PER % 4 == 0, "bins per thread");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int hi = NB - (int)threadIdx.x * PER;  // this thread: bins [hi-PER, hi)
-  uint32_t h[PER];  // h[j] = count of bin hi-1-j
-  if constexpr (PER == 4) {
-    const uint4 v = *reinterpret_cast<const uint4*>(hist + hi - 4);
-    h[0] = v.w;
-    h[1] = v.z;
-    h[2] = v.y;
-    h[3] = v.x;
-  } else {
-    h[0] = hi > 0 ? hist[hi - 1] : 0u;
-  }
   uint32_t local = 0;
+  if constexpr (PER >= 4) {
 #pragma unroll
-  for (int j = 0; j < PER; ++j) local += h[j];
+    for (int u = 0; u < PER / 4; ++u) {
+      const uint4 v = *reinterpret_cast<const uint4*>(hist + hi - PER + 4 * u);
+      local += (v.x + v.y) + (v.z + v.w);
+    }
+  } else {
+    local = hi > 0 ? hist[hi - 1] : 0u;
+  }
   const uint32_t x = warp_incl_scan(local, lane);
   if (lane == 31) sm.ws[warp] = x;
   if (threadIdx.x == 0) sm.bin = 0, sm.above = 0, sm.bin_count = 0;
   __syncthreads();
-  const uint32_t t = sm.ws[lane];
+  const uint32_t t = lane < NT / 32 ? sm.ws[lane] : 0u;
   const uint32_t ti = warp_incl_scan(t, lane);
   uint32_t acc = __shfl_sync(0xffffffffu, ti - t, warp) + x - local;
-  if (acc < k_rem && acc + local >= k_rem) {
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      if (acc < k_rem && acc + h[j] >= k_rem) {
+  if (acc < k_rem && acc + local >= k_rem) {  // the one thread whose bins hold it
+    for (int j = 0; j < PER && hi - 1 - j >= 0; ++j) {
+      const uint32_t h = hist[hi - 1 - j];
+      if (acc + h >= k_rem) {
         sm.bin = (uint32_t)(hi - 1 - j);
         sm.above = acc;
-        sm.bin_count = h[j];
+        sm.bin_count = h;
+        break;
       }
-      acc += h[j];
+      acc += h;
     }
   }
   __syncthreads();
@@ -235,8 +235,8 @@ __device__ __forceinline__ uint32_t shift_in_gt(uint32_t mask, uint32_t a, uint3
 // the next row streams in while this one is selected.  The 128-byte swizzle
 // puts 16-byte piece g of a row at g ^ ((g >> 3) & 7), so the 8 lanes of a
 // quarter-warp reading their consecutive pieces hit distinct banks.
-template <int KPT>
-__global__ void __launch_bounds__(TK_THREADS, 1)
+template <int KPT, int NT>
+__global__ void __launch_bounds__(NT, TK_THREADS / NT)
     topk_reg_kernel(const __grid_constant__ CUtensorMap tm, Shape s, const float* __restrict__ scores,
                     long long ld, long long row_begin, long long rows, int32_t* __restrict__ idx,
                     DevCtx c, int tma_elems) {
@@ -248,7 +248,10 @@ __global__ void __launch_bounds__(TK_THREADS, 1)
   const uint32_t base = smem_u32(dyn_smem);
   uint8_t* aligned = dyn_smem + (((base + 1023u) & ~1023u) - base);
   const float4* stage = reinterpret_cast<const float4*>(aligned);
-  TopkRegSmem& sm = *reinterpret_cast<TopkRegSmem*>(aligned + TK_THREADS * KPT * 4);
+  // the row stage exists only in the 1024-thread form (the others load
+  // directly: two to four of them share an SM)
+  constexpr int STAGE_BYTES = NT == TK_THREADS ? NT * KPT * 4 : 0;
+  TopkRegSmem& sm = *reinterpret_cast<TopkRegSmem*>(aligned + STAGE_BYTES);
   volatile int* abort_flag = &sm.abort_flag;
   const uint32_t bar = smem_u32(&sm.bar), stage_u32 = smem_u32(aligned);
   const int k = s.topk;
@@ -285,12 +288,12 @@ __global__ void __launch_bounds__(TK_THREADS, 1)
     const long long nl = row_len(rl);
     if (nl < 0) {
       if (threadIdx.x == 0) set_status(c, DSA_ERR_INDEX);
-      write_prefix_rows(out, 0, k);
+      write_prefix_rows(out, 0, k, NT);
       issue(rl + gridDim.x);
       continue;
     }
     if (nl <= k) {
-      write_prefix_rows(out, (int)nl, k);
+      write_prefix_rows(out, (int)nl, k, NT);
       issue(rl + gridDim.x);
       continue;
     }
@@ -323,7 +326,7 @@ __global__ void __launch_bounds__(TK_THREADS, 1)
 #pragma unroll
       for (int q = 0; q < KPT; ++q) key[q] = q < nv ? ordered_key(__ldcs(src + e0 + q)) : 0u;
     }
-    for (int i = threadIdx.x; i < 2 * TK_HIST + 256; i += TK_THREADS) sm.hist[i] = 0;
+    for (int i = threadIdx.x; i < 2 * TK_HIST + 256; i += NT) sm.hist[i] = 0;
     if (__syncthreads_or(!ok)) return;  // a stage load that never landed: give up
     // pass 1: bits 31..20 of every key
     uint32_t* h1 = sm.hist;
@@ -336,7 +339,7 @@ __global__ void __launch_bounds__(TK_THREADS, 1)
         if (q < nv) atomicAdd(&h1[key[q] >> 20], 1u);
     }
     __syncthreads();
-    find_bin_2b<TK_HIST>(sm, h1, (uint32_t)k);
+    find_bin_2b<TK_HIST, NT>(sm, h1, (uint32_t)k);
     uint32_t k_rem = (uint32_t)k - sm.above;
     const uint32_t b1 = sm.bin, c1 = sm.bin_count;
     // keys above bin b1 (all taken) and keys in it, as bit masks over q
@@ -353,7 +356,7 @@ __global__ void __launch_bounds__(TK_THREADS, 1)
     if (c1 != k_rem && c1 <= (uint32_t)TK_CAND) {
       // the c1 keys of bin b1 go to shared memory (in index order) and the
       // later passes run over them alone
-      uint32_t off = block_excl_scan_1b((uint32_t)__popc(eqm), sm.ws);
+      uint32_t off = block_excl_scan_1b<NT>((uint32_t)__popc(eqm), sm.ws);
       for (uint32_t m = eqm; m; m &= m - 1u) {
         const int q = __ffs(m) - 1;
         const int g = threadIdx.x * C + (q >> 2);
@@ -364,22 +367,22 @@ __global__ void __launch_bounds__(TK_THREADS, 1)
       __syncthreads();  // candidates complete; the stage is free
       issue(rl + gridDim.x);
       uint32_t* h2 = sm.hist + TK_HIST;
-      for (uint32_t i = threadIdx.x; i < c1; i += TK_THREADS)
+      for (uint32_t i = threadIdx.x; i < c1; i += NT)
         atomicAdd(&h2[(sm.cand[i] >> 8) & 0xFFFu], 1u);
       __syncthreads();
-      find_bin_2b<TK_HIST>(sm, h2, k_rem);
+      find_bin_2b<TK_HIST, NT>(sm, h2, k_rem);
       k_rem -= sm.above;
       uint32_t tp = (b1 << 12) | sm.bin;
       int sh = 8;
       if (sm.bin_count != k_rem) {
         uint32_t* h3 = sm.hist + 2 * TK_HIST;
         const uint32_t b2 = sm.bin;
-        for (uint32_t i = threadIdx.x; i < c1; i += TK_THREADS) {
+        for (uint32_t i = threadIdx.x; i < c1; i += NT) {
           const uint32_t kk = sm.cand[i];
           if (((kk >> 8) & 0xFFFu) == b2) atomicAdd(&h3[kk & 0xFFu], 1u);
         }
         __syncthreads();
-        find_bin_2b<256>(sm, h3, k_rem);
+        find_bin_2b<256, NT>(sm, h3, k_rem);
         k_rem -= sm.above;
         sh = 0;
         tp = (tp << 8) | sm.bin;
@@ -406,7 +409,7 @@ __global__ void __launch_bounds__(TK_THREADS, 1)
       for (int q = 0; q < KPT; ++q)
         if (q < nv && key[q] - lo1 < (1u << 20)) atomicAdd(&h2[(key[q] >> 8) & 0xFFFu], 1u);
       __syncthreads();
-      find_bin_2b<TK_HIST>(sm, h2, k_rem);
+      find_bin_2b<TK_HIST, NT>(sm, h2, k_rem);
       k_rem -= sm.above;
       sh = 8;
       tp = (tp << 12) | sm.bin;
@@ -417,7 +420,7 @@ __global__ void __launch_bounds__(TK_THREADS, 1)
         for (int q = 0; q < KPT; ++q)
           if (q < nv && key[q] - lo2 < 256u) atomicAdd(&h3[key[q] & 0xFFu], 1u);
         __syncthreads();
-        find_bin_2b<256>(sm, h3, k_rem);
+        find_bin_2b<256, NT>(sm, h3, k_rem);
         k_rem -= sm.above;
         sh = 0;
         tp = (tp << 8) | sm.bin;
@@ -436,7 +439,7 @@ __global__ void __launch_bounds__(TK_THREADS, 1)
     }
     const uint32_t take_eq = k_rem;
     const uint32_t p =
-        block_excl_scan_1b((uint32_t)__popc(gtm) | ((uint32_t)__popc(eqm) << 16), sm.ws);
+        block_excl_scan_1b<NT>((uint32_t)__popc(gtm) | ((uint32_t)__popc(eqm) << 16), sm.ws);
     uint32_t gt_b = p & 0xFFFFu, eq_b = p >> 16;
     for (uint32_t m = gtm | eqm; m; m &= m - 1u) {
       const int q = __ffs(m) - 1;
@@ -619,32 +622,56 @@ int launch_topk(const Shape& s, const float* scores, long long ld, long long row
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
     return DSA_ERR_CUDA;
-  const int g = (int)(rows < sms ? rows : sms);
-  const int kpt = max_n <= 4096 ? 4 : max_n <= 8192 ? 8 : max_n <= 16384 ? 16 : 32;
-  // TMA view of each row: S_k / 32 lines of 32 floats (the last S_k % 32
-  // columns, if any, are read directly)
+  // The longest row of this launch sizes the block.  With 1024 threads a row
+  // costs about the same whatever its length (the select's barrier phases
+  // dominate: ~95 us per 1824-row wave at any n), so rows of up to 8192 keys
+  // take 256-thread blocks, four rows per SM (measured per wave: 41 us at
+  // n <= 3648, 68-77 us up to 7296).  512-thread blocks, two rows per SM,
+  // measured slower than 1024 for 8K-16K keys (100-145 us per wave).  Every
+  // thread holds up to 32 keys in registers; the 1024-thread form stages its
+  // next row by TMA.
+  long long n_rows_max = max_n;
+  if (s.q_row_index == nullptr) {
+    const long long b0 = row_begin / s.S_q, b1 = (row_begin + rows - 1) / s.S_q;
+    const long long pmax = s.q_row_offset + (b0 == b1 ? (row_begin + rows - 1) % s.S_q : s.S_q - 1);
+    n_rows_max = pmax + 1 < max_n ? pmax + 1 : max_n;
+    if (n_rows_max < 1) n_rows_max = 1;
+  }
+  const int nt = n_rows_max <= 8192 ? 256 : 1024;
+  int kpt = 32;
+  if (nt == 256) kpt = n_rows_max <= 1024 ? 4 : n_rows_max <= 2048 ? 8 : n_rows_max <= 4096 ? 16 : 32;
+  const long long per_sm = TK_THREADS / nt;
+  const int g = (int)(rows < per_sm * sms ? rows : per_sm * sms);
+  // TMA view of each row (1024-thread form): S_k / 32 lines of 32 floats (the
+  // last S_k % 32 columns, if any, are read directly)
   CUtensorMap tm;
   memset(&tm, 0, sizeof(tm));
   int tma_elems = 0;
-  if ((reinterpret_cast<uintptr_t>(scores) & 15u) == 0 && ld % 4 == 0 && max_n >= 32) {
+  if (nt == TK_THREADS && (reinterpret_cast<uintptr_t>(scores) & 15u) == 0 && ld % 4 == 0 &&
+      max_n >= 32) {
     const uint32_t box_lines = 32 * kpt < 256 ? 32 * kpt : 256;
     if (!make_tmap_f32_lines(&tm, scores, (uint64_t)rows, (uint64_t)ld, (uint64_t)(max_n / 32),
                              box_lines))
       return DSA_ERR_CUDA;
     tma_elems = (max_n / 32) * 32;
   }
-  const size_t smem = 1024 + (size_t)TK_THREADS * kpt * 4 + sizeof(TopkRegSmem);
+  const size_t smem = 1024 + (nt == TK_THREADS ? (size_t)nt * kpt * 4 : 0) + sizeof(TopkRegSmem);
   auto run = [&](auto kernel) -> int {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
+            cudaSuccess ||
+        cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return DSA_ERR_CUDA;
-    kernel<<<g, TK_THREADS, smem, st>>>(tm, s, scores, ld, row_begin, rows, idx, c, tma_elems);
+    kernel<<<g, nt, smem, st>>>(tm, s, scores, ld, row_begin, rows, idx, c, tma_elems);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
   };
-  if (kpt == 4) return run(topk_reg_kernel<4>);
-  if (kpt == 8) return run(topk_reg_kernel<8>);
-  if (kpt == 16) return run(topk_reg_kernel<16>);
-  return run(topk_reg_kernel<32>);
+  if (nt == 256) {
+    if (kpt == 4) return run(topk_reg_kernel<4, 256>);
+    if (kpt == 8) return run(topk_reg_kernel<8, 256>);
+    if (kpt == 16) return run(topk_reg_kernel<16, 256>);
+    return run(topk_reg_kernel<32, 256>);
+  }
+  return run(topk_reg_kernel<32, 1024>);
 }
 
 }  // namespace dsa
