@@ -311,22 +311,27 @@ __global__ void __launch_bounds__(kSThreads, 2)
 }
 
 // --------------------------------- dq ---------------------------------------
-// CTA = (row, 192-column tile of dQ).  dQ[t, :, cols] = sum over key chunks of
-// (scale*dS)[128 heads x 64 keys] * K_sel[64 keys x 192 cols], with scale*dS
-// taken as its bf16 pair hi + lo (two MMAs per chunk on the same K tile).
-// warp 0: MMA; warp 1: TMA of the dS chunks; warps 2..5: gather the 64 kv
-// rows' 192 columns (MN-major SW128: 3 atoms of 64 columns), then the epilogue.
+// CTA = (row, column tile of dQ: [0, 320) or [320, 576)).  dQ[t, :, cols] =
+// sum over key chunks of (scale*dS)[128 heads x 64 keys] * K_sel[64 keys x
+// cols], with scale*dS taken as its bf16 pair hi + lo (two MMAs per chunk on
+// the same K tile: N = 256 + 64 or N = 256).  Two tiles per row (rather than
+// three of 192 columns) read each row's dS chunks twice instead of three
+// times.  warp 0: MMA; warp 1: TMA of the dS chunks; warps 2..5: gather the
+// 64 kv rows' columns (MN-major SW128: 5 or 4 atoms of 64 columns), then the
+// epilogue.
 constexpr int kQStages = 3;
-constexpr int kQN = 192;
+constexpr int kQAtoms = 5;              // 64-column atoms of the wider column tile
+constexpr int kQSplit = 320;            // column tiles [0, 320) and [320, 576)
 struct __align__(1024) DqSmem {
   uint8_t a[kQStages][2][kH * 128];     // dS hi, lo chunks: 128 heads x 64 keys, K-major
-  uint8_t bm[kQStages][3 * 64 * 128];   // 64 keys x 192 cols, MN-major
+  uint8_t bm[kQStages][kQAtoms * 64 * 128];  // 64 keys x up to 320 cols, MN-major
   int32_t idx[2048];
   uint64_t full[kQStages], empty[kQStages], done;
   uint32_t tmem_base;
   int abort;
   int last;
 };
+static_assert(sizeof(DqSmem) + 1024 <= 232448, "dq shared memory");
 
 __global__ void __launch_bounds__(192, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_ds, const __grid_constant__ CUtensorMap tm_dslo,
@@ -335,8 +340,10 @@ __global__ void __launch_bounds__(192, 1)
   extern __shared__ uint8_t smem_raw[];
   DqSmem& sm = *reinterpret_cast<DqSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long row = blockIdx.x / 3;
-  const int nt = blockIdx.x % 3;
+  const long long row = blockIdx.x / 2;
+  const int nt = blockIdx.x % 2;
+  const int col0 = nt == 0 ? 0 : kQSplit;
+  const int natoms = nt == 0 ? kQAtoms : (kDQK - kQSplit) / 64;  // 5 | 4
   const long long b = row / s.S_q;
   const int k = s.topk;
   volatile int* abort_flag = &sm.abort;
@@ -360,7 +367,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   if (last >= 0) atomicMax(&sm.last, last);
   if (warp == 0) {
-    tmem_alloc(smem_u32(&sm.tmem_base), 256);
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);  // 320 columns used
     tmem_relinquish();
     tc_fence_before();
   }
@@ -386,28 +393,29 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp >= 2) {
     const int gw = warp - 2;
-    const __nv_bfloat16* kvb = kv + b * s.S_k * (long long)kDQK + kQN * nt;
+    const __nv_bfloat16* kvb = kv + b * s.S_k * (long long)kDQK + col0;
     for (int ch = 0; ch < nch; ++ch) {
       const int st = ch % kQStages;
       if (!mbar_wait_warp(smem_u32(&sm.empty[st]), ((ch / kQStages) & 1) ^ 1, c, abort_flag)) break;
       // straight into the swizzled stage (cp.async), as in the scores kernel
       const uint32_t bs = smem_u32(sm.bm[st]);
-      if (lane < 24) {
-        const int at = lane >> 3, cc = lane & 7;
+      for (int pc = lane; pc < natoms * 8; pc += 32) {  // 16-byte piece pc of the tile's row
+        const int at = pc >> 3, cc = pc & 7;
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
           const int key = gw + 4 * m;
           const int sl = 64 * ch + key;
           const int id = (sl < k && sm.idx[sl] >= 0) ? sm.idx[sl] : 0;
           cp_async16_cg(bs + at * 8192 + key * 128 + ((cc ^ (key & 7)) << 4),
-                        reinterpret_cast<const uint4*>(kvb + (long long)id * kDQK) + lane);
+                        reinterpret_cast<const uint4*>(kvb + (long long)id * kDQK) + pc);
         }
       }
       cp_async_arrive_noinc(smem_u32(&sm.full[st]));
     }
     cp_async_wait_all();  // no copy may still be in flight when the CTA exits
   } else if (lane == 0) {
-    constexpr uint32_t idesc = idesc_bf16(128, kQN, false, true);
+    constexpr uint32_t idesc256 = idesc_bf16(128, 256, false, true);
+    constexpr uint32_t idesc64 = idesc_bf16(128, 64, false, true);
     for (int ch = 0; ch < nch; ++ch) {
       const int st = ch % kQStages;
       if (!mbar_wait(smem_u32(&sm.full[st]), (ch / kQStages) & 1, c, abort_flag)) break;
@@ -418,10 +426,14 @@ __global__ void __launch_bounds__(192, 1)
       for (int hl = 0; hl < 2; ++hl) {
         const uint32_t a0 = smem_u32(sm.a[st][hl]);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ss(tmem, sdesc(a0 + kk * 32, 16, 1024, kSw128),
-                      sdesc(b0 + kk * 2048, 8192, 1024, kSw128), idesc,
-                      (ch > 0 || hl > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ad = sdesc(a0 + kk * 32, 16, 1024, kSw128);
+          const uint32_t acc = (ch > 0 || hl > 0 || kk > 0) ? 1u : 0u;
+          mma_bf16_ss(tmem, ad, sdesc(b0 + kk * 2048, 8192, 1024, kSw128), idesc256, acc);
+          if (natoms == kQAtoms)  // the fifth atom: columns 256..319 of the tile
+            mma_bf16_ss(tmem + 256, ad, sdesc(b0 + 4 * 8192 + kk * 2048, 8192, 1024, kSw128), idesc64,
+                        acc);
+        }
       }
       mma_commit(smem_u32(&sm.empty[st]));
     }
@@ -432,9 +444,9 @@ __global__ void __launch_bounds__(192, 1)
     const int h = quad * 32 + lane;
     bool have = nch > 0 && mbar_wait_warp(smem_u32(&sm.done), 0, c, abort_flag);
     tc_fence_after();
-    __nv_bfloat16* dst = dq + (row * kH + h) * (long long)kDQK + kQN * nt;
+    __nv_bfloat16* dst = dq + (row * kH + h) * (long long)kDQK + col0;
 #pragma unroll 1
-    for (int cc = 0; cc < kQN; cc += 32) {
+    for (int cc = 0; cc < natoms * 64; cc += 32) {
       uint32_t v[32];
       if (have) {
         tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + cc, v);
@@ -456,7 +468,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -765,7 +777,7 @@ int launch_attn_bwd_tc(const Shape& s, const void* q, const void* kv, const int3
   scores_kernel<true><<<(unsigned)(rows * ntile), kSThreads, s1, st>>>(
       tq, tdo, (const __nv_bfloat16*)kv, s, idx, mx, sm, D, P_ws, Plo_ws, dS_ws, dSlo_ws, praw,
       ntile, c);
-  dq_kernel<<<(unsigned)(rows * 3), 192, s2, st>>>(tds, tdslo, (const __nv_bfloat16*)kv, s, idx,
+  dq_kernel<<<(unsigned)(rows * 2), 192, s2, st>>>(tds, tdslo, (const __nv_bfloat16*)kv, s, idx,
                                                     (__nv_bfloat16*)dq, c);
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
