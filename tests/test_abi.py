@@ -114,3 +114,33 @@ def test_backward_workspace_sizes():
     # the tensor-core backward needs its workspace
     assert dsa.lib.dsa_sparse_attn_bwd(ctypes.byref(p), 16, 16, 16, 16, 16, 16, 16, 16, 16, None,
                                        None) == dsa.DSA_ERR_WORKSPACE
+
+
+def test_fused_indexer_topk_workspace_and_rejections():
+    # dsa_indexer_topk (and dsa_forward with DSA_FLAG_FUSED_TOPK) keep one
+    # wave's candidate lists: keys and positions (4 bytes each per key) and a
+    # count per row; bf16 DeepSeek indexer shapes with S_k < 65536 only
+    dsa = _lib()
+    mk = lambda **kw: dsa.make_params(**dict(dict(B=1, S_q=64, S_k=64, H=128, d_qk=576, d_v=512,
+                                                  H_I=64, d_I=128, topk=16, scale=0.5, dtype="bf16",
+                                                  wave_rows=64), **kw))
+    p = mk()
+    W, S = 64, 64
+    need = 2 * W * S * 4 + W * 4
+    assert dsa.workspace_size(p, dsa.DSA_CALL_INDEXER_TOPK) >= need
+    assert dsa.workspace_size(mk(flags=dsa.DSA_FLAG_FUSED_TOPK), dsa.DSA_CALL_FORWARD) >= need
+    # the plain forward's ring is unchanged by the new call
+    assert dsa.workspace_size(p, dsa.DSA_CALL_FORWARD) == W * S * 4
+    # unsupported: fp32, other indexer shapes, S_k >= 65536, with the FP8 flag
+    for bad in (mk(dtype="fp32"), mk(H_I=32), mk(S_k=65536, S_q=64),
+                mk(flags=dsa.DSA_FLAG_FUSED_TOPK | dsa.DSA_FLAG_FP8_INDEXER)):
+        assert dsa.workspace_size(bad, dsa.DSA_CALL_INDEXER_TOPK) == 0
+        assert dsa.lib.dsa_indexer_topk(ctypes.byref(bad), 16, 16, 16, 0, 1, 16, 16, None) == \
+            dsa.DSA_ERR_UNSUPPORTED
+    # argument checks happen on the host, before any launch
+    assert dsa.lib.dsa_indexer_topk(ctypes.byref(p), 16, 16, 16, 0, 65, 16, 16, None) == \
+        dsa.DSA_ERR_INVALID_ARG
+    assert dsa.lib.dsa_indexer_topk(ctypes.byref(p), 16, 16, 16, 0, 1, 16, None, None) == \
+        dsa.DSA_ERR_WORKSPACE
+    assert dsa.lib.dsa_forward_static_ws(ctypes.byref(mk(flags=dsa.DSA_FLAG_FUSED_TOPK)),
+                                         *([16] * 9), None) == dsa.DSA_ERR_UNSUPPORTED
