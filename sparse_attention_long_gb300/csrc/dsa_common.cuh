@@ -377,24 +377,54 @@ __device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
 }
 
-// Lightning Indexer head reduction of one score: sum_j w[j] * max(x_j, 0)
-// over 64 heads, x_j = v0[j] (j < 32) or v1[j - 32] as fp32 bits, w in
-// shared memory (16-byte aligned).  Four running sums (heads j mod 4),
-// advanced two at a time by packed FMAs, then (s0 + s1) + (s2 + s3).
-__device__ __forceinline__ float relu_wsum64(const uint32_t (&v0)[32], const uint32_t (&v1)[32],
-                                             const float* w) {
-  uint64_t a01 = 0, a23 = 0;  // two +0.0f each
+// Half of the Lightning Indexer head reduction: heads h0 .. h0+31 (x in v,
+// weights w[0..31]) added to the four running sums (heads j mod 4).
+__device__ __forceinline__ void relu_acc32(const uint32_t (&v)[32], const float* w, uint64_t& a01,
+                                           uint64_t& a23) {
 #pragma unroll
-  for (int h = 0; h < 64; h += 4) {
-    const uint32_t* v = h < 32 ? v0 + h : v1 + (h - 32);
+  for (int h = 0; h < 32; h += 4) {
     const float4 wa = *reinterpret_cast<const float4*>(w + h);
-    a01 = ffma2(wa.x, wa.y, fmaxf(__uint_as_float(v[0]), 0.f), fmaxf(__uint_as_float(v[1]), 0.f), a01);
-    a23 = ffma2(wa.z, wa.w, fmaxf(__uint_as_float(v[2]), 0.f), fmaxf(__uint_as_float(v[3]), 0.f), a23);
+    a01 = ffma2(wa.x, wa.y, fmaxf(__uint_as_float(v[h]), 0.f), fmaxf(__uint_as_float(v[h + 1]), 0.f), a01);
+    a23 = ffma2(wa.z, wa.w, fmaxf(__uint_as_float(v[h + 2]), 0.f), fmaxf(__uint_as_float(v[h + 3]), 0.f), a23);
   }
+}
+__device__ __forceinline__ float relu_sum_finish(uint64_t a01, uint64_t a23) {
   float a0, a1, a2, a3;
   unpack2(a01, a0, a1);
   unpack2(a23, a2, a3);
   return (a0 + a1) + (a2 + a3);
+}
+
+// Lightning Indexer head reduction, sum_j w[j] * max(x_j, 0) over 64 heads,
+// for the indexer epilogue's two tokens of one key block (lane = key): token
+// 0's score from TMEM columns tb .. tb+63 (weights w0), token 1's from
+// tb+64 .. tb+127 (w1).  Four running sums (heads j mod 4), advanced two at
+// a time by packed FMAs, then (s0 + s1) + (s2 + s3).  The four 32-column
+// pieces go through the caller's two register buffers A and B, so the next
+// piece's TMEM load is in flight while the current piece is reduced; the
+// first call returns token 0's score with token 1's first piece still
+// loading (so its store overlaps that load), the second call token 1's.
+__device__ __forceinline__ float relu_pair_first(uint32_t tb, const float* w0, uint32_t (&A)[32],
+                                                 uint32_t (&B)[32]) {
+  uint64_t a01 = 0, a23 = 0;
+  tmem_ld32(tb, A);
+  tmem_ld_wait(A);
+  tmem_ld32(tb + 32, B);
+  relu_acc32(A, w0, a01, a23);
+  tmem_ld_wait(B);
+  tmem_ld32(tb + 64, A);
+  relu_acc32(B, w0 + 32, a01, a23);
+  return relu_sum_finish(a01, a23);
+}
+__device__ __forceinline__ float relu_pair_second(uint32_t tb, const float* w1, uint32_t (&A)[32],
+                                                  uint32_t (&B)[32]) {
+  uint64_t a01 = 0, a23 = 0;
+  tmem_ld_wait(A);
+  tmem_ld32(tb + 96, B);
+  relu_acc32(A, w1, a01, a23);
+  tmem_ld_wait(B);
+  relu_acc32(B, w1 + 32, a01, a23);
+  return relu_sum_finish(a01, a23);
 }
 
 // Shared-memory matrix descriptor (tcgen05): start, leading / stride byte

@@ -181,18 +181,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const long long key = (long long)kb * kBK + quad * 32 + lane;
       const float skey = key < s.S_k ? k_scale[(long long)batch * s.S_k + key] : 0.f;
+      // both tokens of the warp (2*half, 2*half+1): pipelined TMEM loads
+      const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + acc * kN + half * 2 * kHI;
+      uint32_t A[32], B[32];
 #pragma unroll
       for (int tt = 0; tt < 2; ++tt) {
         const int j = half * 2 + tt;
-        const long long p = sm.pos[j];
-        if (p < (long long)kb * kBK) continue;  // whole block masked for this row (warp-uniform)
-        const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + acc * kN + j * kHI;
-        uint32_t v0[32], v1[32];
-        tmem_ld32(ta, v0);
-        tmem_ld32(ta + 32, v1);
-        tmem_ld_wait(v0);
-        tmem_ld_also(v1);
-        if (key <= p) scores[(r0 + j - row_begin) * ld + key] = skey * relu_wsum64(v0, v1, sm.w[j]);
+        const float sc = tt == 0 ? relu_pair_first(tb, sm.w[j], A, B) : relu_pair_second(tb, sm.w[j], A, B);
+        if (key <= sm.pos[j]) scores[(r0 + j - row_begin) * ld + key] = skey * sc;
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.acc_empty[acc]));

@@ -209,18 +209,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kFused && !ok_w && lane == 0) sm.grp_fail[half] = 1;  // read at the next update
       tc_fence_after();
       const long long key = (long long)kb * kBK + quad * 32 + lane;
+      // both tokens of the warp (2*half, 2*half+1): pipelined TMEM loads
+      const int j0 = half * 2;
+      const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + acc * kN + j0 * kHI;
+      uint32_t A[32], B[32];
 #pragma unroll
       for (int tt = 0; tt < 2; ++tt) {
-        const int j = half * 2 + tt;
+        const int j = j0 + tt;
         const long long p = sm.pos[j];
+        float score = 0.f;
+        if (ok_w) score = tt == 0 ? relu_pair_first(tb, sm.w[j0], A, B) : relu_pair_second(tb, sm.w[j], A, B);
         if (!ok_w || p < (long long)kb * kBK) continue;  // whole block masked for this row (warp-uniform)
-        const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + acc * kN + j * kHI;
-        uint32_t v0[32], v1[32];
-        tmem_ld32(ta, v0);
-        tmem_ld32(ta + 32, v1);
-        tmem_ld_wait(v0);
-        tmem_ld_also(v1);
-        const float score = relu_wsum64(v0, v1, sm.w[j]);
         if (!kFused) {
           if (key <= p) scores[(r0 + j - row_begin) * ld + key] = score;
         } else if (p >= k) {  // rows with at most k visible keys take all of them: no list
@@ -246,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (kFused && ((kb & (kUpdateEvery - 1)) == kUpdateEvery - 1 || kb == nkb - 1)) {
         // every kUpdateEvery blocks: the group's candidates so far are
-        // counted; one thread raises the two tokens' thresholds while the
+        // counted; one warp raises the two tokens' thresholds while the
         // group waits (a warp whose wait failed keeps walking the blocks
         // without work until here, so the group leaves together)
         named_bar_sync(2 + half, 128);
