@@ -74,3 +74,24 @@ def test_heavy_ties_long_row():
     sc[1] = 1.0
     sc[2, ::2] = -0.0
     _check(dsa, sc, [S_k - 1, S_k - 1, S_k - 1, 5000, 30000, 2047, 2048, 12345], k)
+
+
+@pytest.mark.parametrize("values", [1, 3, 1000])
+def test_sized_blocks_rows_up_to_8k(values):
+    # rows addressed by offset (no q_row_index), all shorter than 8193 keys, so
+    # the launch takes the 256-thread form with 32 keys per thread; with one
+    # value the threshold's bin holds every key (> 4096: the passes run over
+    # registers), with 3 about 2,700 (the candidate list), with 1000 a few
+    dsa = lib()
+    S_k, k, r0, rows = 8192, 2048, 8192 - 96, 96
+    p = dsa.make_params(B=1, S_q=S_k, S_k=S_k, H=1, d_qk=8, d_v=8, H_I=1, d_I=8, topk=k, scale=1.0,
+                        dtype="fp32")
+    rng = np.random.default_rng(values)
+    sc = rng.integers(0, values, size=(rows, S_k)).astype(np.float32)
+    got = torch.full((rows, k), -7, dtype=torch.int32, device=DEV)
+    dsa.topk(p, torch.as_tensor(sc, device=DEV), r0, rows, got)
+    torch.cuda.synchronize()
+    assert dsa.get_status() == 0
+    ref = topk_select(sc[None], np.arange(r0, r0 + rows)[None], k)[0]
+    bad = np.nonzero((got.cpu().numpy() != ref).any(axis=1))[0]
+    assert bad.size == 0, f"{bad.size} rows differ, first row {bad[:3]}"
