@@ -143,6 +143,7 @@ struct TopkRegSmem {
   uint32_t cand[TK_CAND];            // keys of the threshold's pass-1 bin
   uint32_t ws[TK_WARPS];
   uint32_t bin, above, bin_count;
+  uint32_t n_cand;  // candidate slots handed out so far (this row)
   int abort_flag;
   unsigned long long bar;  // stage-full barrier (8-byte aligned by the layout)
 };
@@ -266,8 +267,11 @@ __global__ void __launch_bounds__(NT, TK_THREADS / NT)
     return (pos < 0 || pos >= s.S_k) ? -1 : pos + 1;
   };
   auto loads_row = [&](long long rl) { return tma_elems > 0 && rl < rows && row_len(rl) > k; };
-  auto issue = [&](long long rl) {  // thread 0: stage row rl if it is selected from
-    if (threadIdx.x != 0 || !loads_row(rl)) return;
+  // The block's last thread stages rows: it holds no keys of rows shorter
+  // than NT * KPT - KPT and no pass-2 candidate while the threshold's bin
+  // holds fewer than NT keys, so the copy is issued off the barrier chain.
+  auto issue = [&](long long rl) {  // stage row rl if it is selected from
+    if (threadIdx.x != NT - 1 || !loads_row(rl)) return;
     const int nn = (int)row_len(rl);
     const int nbox = (min(nn, tma_elems) + BOX_ELEMS - 1) / BOX_ELEMS;
     fence_proxy_async_smem();  // the stage's earlier reads come before these writes
@@ -327,6 +331,7 @@ __global__ void __launch_bounds__(NT, TK_THREADS / NT)
       for (int q = 0; q < KPT; ++q) key[q] = q < nv ? ordered_key(__ldcs(src + e0 + q)) : 0u;
     }
     for (int i = threadIdx.x; i < 2 * TK_HIST + 256; i += NT) sm.hist[i] = 0;
+    if (threadIdx.x == 0) sm.n_cand = 0;
     if (__syncthreads_or(!ok)) return;  // a stage load that never landed: give up
     // pass 1: bits 31..20 of every key
     uint32_t* h1 = sm.hist;
@@ -354,9 +359,17 @@ __global__ void __launch_bounds__(NT, TK_THREADS / NT)
     gtm = (__brev(gtm) >> (32 - KPT)) & vmask;
     eqm = (__brev(eqm) >> (32 - KPT)) & ~gtm & vmask;
     if (c1 != k_rem && c1 <= (uint32_t)TK_CAND) {
-      // the c1 keys of bin b1 go to shared memory (in index order) and the
-      // later passes run over them alone
-      uint32_t off = block_excl_scan_1b<NT>((uint32_t)__popc(eqm), sm.ws);
+      // the c1 keys of bin b1 go to shared memory and the later passes run
+      // over them alone; each thread's keys take consecutive slots (one
+      // shared counter bumped once per warp), the order across threads is
+      // immaterial: the passes only count them, and each thread re-reads its
+      // own to classify them
+      const int lane = threadIdx.x & 31;
+      const uint32_t mine = (uint32_t)__popc(eqm);
+      const uint32_t incl = warp_incl_scan(mine, lane);
+      uint32_t wbase = 0;
+      if (lane == 31 && incl > 0) wbase = atomicAdd(&sm.n_cand, incl);
+      uint32_t off = __shfl_sync(0xffffffffu, wbase, 31) + incl - mine;
       for (uint32_t m = eqm; m; m &= m - 1u) {
         const int q = __ffs(m) - 1;
         const int g = threadIdx.x * C + (q >> 2);
@@ -628,8 +641,9 @@ int launch_topk(const Shape& s, const float* scores, long long ld, long long row
   // take 256-thread blocks, four rows per SM (measured per wave: 41 us at
   // n <= 3648, 68-77 us up to 7296).  512-thread blocks, two rows per SM,
   // measured slower than 1024 for 8K-16K keys (100-145 us per wave).  Every
-  // thread holds up to 32 keys in registers; the 1024-thread form stages its
-  // next row by TMA.
+  // thread holds up to 32 keys in registers (16 in the 1024-thread form for
+  // rows of up to 16384 keys, so twice as many threads share each pass); the
+  // 1024-thread form stages its next row by TMA.
   long long n_rows_max = max_n;
   if (s.q_row_index == nullptr) {
     const long long b0 = row_begin / s.S_q, b1 = (row_begin + rows - 1) / s.S_q;
@@ -638,7 +652,7 @@ int launch_topk(const Shape& s, const float* scores, long long ld, long long row
     if (n_rows_max < 1) n_rows_max = 1;
   }
   const int nt = n_rows_max <= 8192 ? 256 : 1024;
-  int kpt = 32;
+  int kpt = nt == TK_THREADS && n_rows_max <= 16384 ? 16 : 32;
   if (nt == 256) kpt = n_rows_max <= 1024 ? 4 : n_rows_max <= 2048 ? 8 : n_rows_max <= 4096 ? 16 : 32;
   const long long per_sm = TK_THREADS / nt;
   const int g = (int)(rows < per_sm * sms ? rows : per_sm * sms);
@@ -671,6 +685,7 @@ int launch_topk(const Shape& s, const float* scores, long long ld, long long row
     if (kpt == 16) return run(topk_reg_kernel<16, 256>);
     return run(topk_reg_kernel<32, 256>);
   }
+  if (kpt == 16) return run(topk_reg_kernel<16, 1024>);
   return run(topk_reg_kernel<32, 1024>);
 }
 

@@ -76,18 +76,25 @@ def test_heavy_ties_long_row():
     _check(dsa, sc, [S_k - 1, S_k - 1, S_k - 1, 5000, 30000, 2047, 2048, 12345], k)
 
 
-@pytest.mark.parametrize("values", [1, 3, 1000])
-def test_sized_blocks_rows_up_to_8k(values):
-    # rows addressed by offset (no q_row_index), all shorter than 8193 keys, so
-    # the launch takes the 256-thread form with 32 keys per thread; with one
+@pytest.mark.parametrize("S_k", [8192, 16384])
+@pytest.mark.parametrize("values", [1, 3, 1000, 0])
+def test_sized_blocks_offset_rows(S_k, values):
+    # rows addressed by offset (no q_row_index), so the launch sizes its
+    # blocks by the longest row: up to 8192 keys the 256-thread form with 32
+    # keys per thread, up to 16384 the 1024-thread form with 16.  With one
     # value the threshold's bin holds every key (> 4096: the passes run over
-    # registers), with 3 about 2,700 (the candidate list), with 1000 a few
+    # registers), with 3 a third of them (the candidate list at 8192, registers
+    # at 16384), with 1000 a few hundred, with 0 normal scores
     dsa = lib()
-    S_k, k, r0, rows = 8192, 2048, 8192 - 96, 96
+    k, rows = 2048, 96
+    r0 = S_k - rows
     p = dsa.make_params(B=1, S_q=S_k, S_k=S_k, H=1, d_qk=8, d_v=8, H_I=1, d_I=8, topk=k, scale=1.0,
                         dtype="fp32")
-    rng = np.random.default_rng(values)
-    sc = rng.integers(0, values, size=(rows, S_k)).astype(np.float32)
+    rng = np.random.default_rng(values + S_k)
+    if values:
+        sc = rng.integers(0, values, size=(rows, S_k)).astype(np.float32)
+    else:
+        sc = synth.normal((rows, S_k), 11, seed=2, dtype=torch.float32).numpy() * 8.0
     got = torch.full((rows, k), -7, dtype=torch.int32, device=DEV)
     dsa.topk(p, torch.as_tensor(sc, device=DEV), r0, rows, got)
     torch.cuda.synchronize()
