@@ -93,7 +93,18 @@ __device__ __forceinline__ void find_bin(TopkSmem& sm, int nbins, uint32_t k_rem
   __syncthreads();
 }
 
+// A row with n <= k visible keys takes all of them: out = 0, 1, ..., n-1,
+// then -1 (16-byte stores when the row allows them).
 __device__ __forceinline__ void write_prefix_rows(int32_t* out, int n, int k, int nt = TK_THREADS) {
+  if ((k & 3) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
+    for (int j = threadIdx.x; j < k / 4; j += nt) {
+      const int b = 4 * j;
+      const int4 v = make_int4(b < n ? b : -1, b + 1 < n ? b + 1 : -1, b + 2 < n ? b + 2 : -1,
+                               b + 3 < n ? b + 3 : -1);
+      reinterpret_cast<int4*>(out)[j] = v;
+    }
+    return;
+  }
   for (int j = threadIdx.x; j < k; j += nt) out[j] = j < n ? j : -1;
 }
 
