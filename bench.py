@@ -18,6 +18,7 @@ step.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -234,21 +235,41 @@ def topk_stage(dsa, dev, wl, steps, warmup, peaks):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks / throttle reasons, sampled every 50 ms from before
+    the warm-up on; only the samples stamped inside the timed region count."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
         self.index = index
+        self.t0 = self.t1 = None
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                       "--format=csv,noheader,nounits", "-lms", "50"],
                                       stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.p = None
+        # wait (at most 5 s) for the first sample, so the sampler runs when
+        # the timed region starts
+        t_end = time.time() + 5.0
+        while self.p is not None and time.time() < t_end and os.path.getsize(self.f.name) == 0:
+            time.sleep(0.02)
+
+    def start_window(self):
+        self.t0 = time.time()
+
+    def end_window(self):
+        self.t1 = time.time()
+
+    @staticmethod
+    def _stamp(text):
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
 
     def stop(self):
         if self.p is None:
@@ -259,16 +280,21 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.p.kill()
         self.f.seek(0)
-        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.count(",") >= 8]
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.count(",") >= 9]
         os.unlink(self.f.name)
+        inside = [r for r in rows if self.t0 is not None and self.t1 is not None and
+                  (ts := self._stamp(r[0])) is not None and self.t0 <= ts <= self.t1]
+        window = bool(inside)
+        rows = inside if inside else rows
         if not rows:
             return None
-        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        sm = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].strip().replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].strip() == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
+                "samples_in_timed_region": window}
 
 
 def kernel_traffic(kernel_file, summary):
@@ -492,6 +518,7 @@ def main():
         dsa.sparse_attn_fwd(p, x["q"], x["kv"], idx, out, m, l)
         if ev: ev["attn"][1].record(stream)
 
+    clocks = ClockSampler(local)
     for _ in range(args.warmup):
         step()
         flush.zero_()
@@ -501,16 +528,17 @@ def main():
     E = lambda: torch.cuda.Event(enable_timing=True)
     evs = [dict(idx=[(E(), E()) for _ in waves], topk=[(None, E()) for _ in waves], attn=(E(), E()))
            for _ in range(args.steps)]
-    clocks = ClockSampler(local)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    clocks.start_window()
     t_wall = time.perf_counter()
     for s in range(args.steps):
         step(evs[s])
         flush.zero_()          # L2 flush between steps (outside the per-stage events)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
+    clocks.end_window()
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
