@@ -662,15 +662,16 @@ int launch_topk(const Shape& s, const float* scores, long long ld, long long row
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
     return DSA_ERR_CUDA;
-  // The longest row of this launch sizes the block.  With 1024 threads a row
-  // costs about the same whatever its length (the select's barrier phases
-  // dominate: ~95 us per 1824-row wave at any n), so rows of up to 8192 keys
-  // take 256-thread blocks, four rows per SM (measured per wave: 41 us at
-  // n <= 3648, 68-77 us up to 7296).  512-thread blocks, two rows per SM,
-  // measured slower than 1024 for 8K-16K keys (100-145 us per wave).  Every
-  // thread holds up to 32 keys in registers (16 in the 1024-thread form for
-  // rows of up to 16384 keys, so twice as many threads share each pass); the
-  // 1024-thread form stages its next row by TMA.
+  // The longest row of this launch sizes the block.  Rows of up to 4096 keys
+  // take 256-thread blocks, four rows per SM (measured per 1824-row wave:
+  // 45 us at n <= 3648); longer rows one 1024-thread block per SM, whose
+  // cost per row hardly depends on the row's length (the select's barrier
+  // phases dominate), so the keys are spread over all 1024 threads: 8 per
+  // thread up to 8192 keys (67-69 us per wave against 72-86 us for 256-thread
+  // blocks with 32 each), 16 up to 16384 (78-84 us against 103-106 us with
+  // 32), 32 beyond.  512-thread blocks, two rows per SM, measured slower than
+  // 1024 for 8K-16K keys (100-145 us per wave).  The 1024-thread form stages
+  // its next row by TMA.
   long long n_rows_max = max_n;
   if (s.q_row_index == nullptr) {
     const long long b0 = row_begin / s.S_q, b1 = (row_begin + rows - 1) / s.S_q;
@@ -678,9 +679,9 @@ int launch_topk(const Shape& s, const float* scores, long long ld, long long row
     n_rows_max = pmax + 1 < max_n ? pmax + 1 : max_n;
     if (n_rows_max < 1) n_rows_max = 1;
   }
-  const int nt = n_rows_max <= 8192 ? 256 : 1024;
-  int kpt = nt == TK_THREADS && n_rows_max <= 16384 ? 16 : 32;
-  if (nt == 256) kpt = n_rows_max <= 1024 ? 4 : n_rows_max <= 2048 ? 8 : n_rows_max <= 4096 ? 16 : 32;
+  const int nt = n_rows_max <= 4096 ? 256 : 1024;
+  int kpt = n_rows_max <= 8192 ? 8 : n_rows_max <= 16384 ? 16 : 32;
+  if (nt == 256) kpt = n_rows_max <= 1024 ? 4 : n_rows_max <= 2048 ? 8 : 16;
   const long long per_sm = TK_THREADS / nt;
   const int g = (int)(rows < per_sm * sms ? rows : per_sm * sms);
   // TMA view of each row (1024-thread form): S_k / 32 lines of 32 floats (the
@@ -709,9 +710,9 @@ int launch_topk(const Shape& s, const float* scores, long long ld, long long row
   if (nt == 256) {
     if (kpt == 4) return run(topk_reg_kernel<4, 256>);
     if (kpt == 8) return run(topk_reg_kernel<8, 256>);
-    if (kpt == 16) return run(topk_reg_kernel<16, 256>);
-    return run(topk_reg_kernel<32, 256>);
+    return run(topk_reg_kernel<16, 256>);
   }
+  if (kpt == 8) return run(topk_reg_kernel<8, 1024>);
   if (kpt == 16) return run(topk_reg_kernel<16, 1024>);
   return run(topk_reg_kernel<32, 1024>);
 }

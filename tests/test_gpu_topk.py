@@ -76,15 +76,15 @@ def test_heavy_ties_long_row():
     _check(dsa, sc, [S_k - 1, S_k - 1, S_k - 1, 5000, 30000, 2047, 2048, 12345], k)
 
 
-@pytest.mark.parametrize("S_k", [8192, 16384])
+@pytest.mark.parametrize("S_k", [4096, 8192, 16384])
 @pytest.mark.parametrize("values", [1, 3, 1000, 0])
 def test_sized_blocks_offset_rows(S_k, values):
     # rows addressed by offset (no q_row_index), so the launch sizes its
-    # blocks by the longest row: up to 8192 keys the 256-thread form with 32
-    # keys per thread, up to 16384 the 1024-thread form with 16.  With one
-    # value the threshold's bin holds every key (> 4096: the passes run over
-    # registers), with 3 a third of them (the candidate list at 8192, registers
-    # at 16384), with 1000 a few hundred, with 0 normal scores
+    # blocks by the longest row: up to 4096 keys the 256-thread form (16 keys
+    # per thread), up to 8192 the 1024-thread form with 8, up to 16384 with
+    # 16.  With one value the threshold's bin holds every key (the passes run
+    # over registers once it exceeds the 4096-entry list), with 3 a third of
+    # them, with 1000 a few dozen to a few hundred, with 0 normal scores
     dsa = lib()
     k, rows = 2048, 96
     r0 = S_k - rows
