@@ -286,6 +286,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     sm.abort = 0;
     fence_mbar_init();
   }
+  {
+    // the block stages start as zeros (slots that are never gathered stay finite)
+    uint4* z = reinterpret_cast<uint4*>(&sm.stage[0][0]);
+    for (int i = threadIdx.x; i < kStages * kStageBytes / 16; i += kThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();  // generic writes -> the tensor cores' reads
+  }
   if (warp == 0) {
     tmem_alloc2(smem_u32(&sm.tmem_base), kTmemCols);
     tmem_relinquish2();
@@ -340,8 +346,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // [128c, 128c+128), lanes 16..31 those of [256+128c, 256+128c+128), into
     // value chunks 0..3 (SW128 rows).  Rope: 8 slots per copy, 4 lanes per
     // slot, the 64 bytes of columns R_c into the rope chunk (SW64 rows).
-    // Invalid slots copy row 0, so every byte the MMAs read is finite (their
-    // P is 0).
+    // Invalid slots (past the token's k entries, -1 or out of range) are not
+    // copied: they keep an earlier block's row or the zeros the stages start
+    // with, so every byte the MMAs read is finite, and their P is 0.  (Copying
+    // row 0 for them sent ~80 copies of one row per CTA to the same L2 lines
+    // at every token's last block and made that block's gather ~3x slower.)
     const int gw = warp - kWarpGather0;
     const int run = lane >> 4, p16 = lane & 15;
     const int vcol = 256 * run + 128 * (int)crank + 8 * p16;   // this lane's value piece
@@ -419,7 +428,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // this warp's 28 indices of the block (loaded before the wait)
         const int e = j * kBlk + kSlotsPerWarp * gw + lane;
         int id = (lane < kSlotsPerWarp && e < k) ? irow[e] : -1;
-        if (id < 0 || id >= s.S_k) id = 0;
+        if (id >= s.S_k) id = -1;
         if (!mbar_wait_warp(smem_u32(&sm.st_empty[st]), ((G / kStages) & 1) ^ 1, c, abort_flag)) {
           ok = false;
           break;
@@ -429,15 +438,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int t = 0; t < kSlotsPerWarp; ++t) {
           const int r = kSlotsPerWarp * gw + t;
           const int rid = __shfl_sync(0xffffffffu, id, t);
-          cp_async16_cg(base + vchunk * kChunk + r * 128 + ((vpc ^ (r & 7)) << 4),
-                        kvb + (long long)rid * kDQK + vcol);
+          if (rid >= 0)
+            cp_async16_cg(base + vchunk * kChunk + r * 128 + ((vpc ^ (r & 7)) << 4),
+                          kvb + (long long)rid * kDQK + vcol);
         }
 #pragma unroll
         for (int g8 = 0; g8 < 4; ++g8) {
           const int rl = 8 * g8 + rs;
           const int rid = __shfl_sync(0xffffffffu, id, rl & 31);
           const int r = kSlotsPerWarp * gw + rl;
-          if (rl < kSlotsPerWarp)
+          if (rl < kSlotsPerWarp && rid >= 0)
             cp_async16_cg(base + 4 * kChunk + r * 64 + ((rp ^ ((r >> 1) & 3)) << 4),
                           kvb + (long long)rid * kDQK + rcol);
         }
