@@ -201,17 +201,27 @@ def backward_stage(dsa, dev, steps, peak_tc, workload="dsv32_S16384_train", rows
     t_bwd = time_calls(bwd, steps, 1, stream)
     t_kl = time_calls(kl, steps, 1, stream)
     t_both = time_calls(both, steps, 1, stream)
+    # dsa_backward in row passes (wave_rows): the workspace holds one pass
+    W = min(2048, S_q)
+    p_w = dsa.make_params(B=1, S_q=S_q, S_k=S, H=H, d_qk=wl["d_qk"], d_v=wl["d_v"], H_I=wl["H_I"],
+                          d_I=wl["d_I"], topk=k, scale=wl["scale"], dtype="bf16",
+                          q_row_offset=S - S_q, wave_rows=W)
+    ws_w = torch.empty(dsa.workspace_size(p_w, dsa.DSA_CALL_BACKWARD), dtype=torch.uint8, device=dev)
+    both_w = lambda: dsa.backward(p_w, x["q"], x["kv"], idx, out, x["dO"], m, l, x["q_I"], x["k_I"],
+                                  x["w"], dq, dkv, loss, dq_I, dk_I, dw, ws_w)
+    t_both_w = time_calls(both_w, steps, 1, stream)
     assert dsa.get_status() == 0, "device status after the backward"
     f_bwd, f_kl = algorithmic_bwd(wl, np.arange(S - S_q, S))
     return {"workload": wl["name"], "rows": S_q, "calls_timed": steps,
             "forward_ms": t_fwd, "attn_bwd_ms": t_bwd, "kl_bwd_ms": t_kl,
             "backward_ms": t_both,
+            "backward_ms_in_passes": t_both_w, "pass_rows": W,
             "backward_tflops": (f_bwd + f_kl) / (t_both * 1e-3) / 1e12,
             "attn_bwd_tflops": f_bwd / (t_bwd * 1e-3) / 1e12,
             "kl_bwd_tflops": f_kl / (t_kl * 1e-3) / 1e12,
             "attn_bwd_frac": f_bwd / (t_bwd * 1e-3) / 1e12 / peak_tc,
             "workspace_bytes": {"attn_bwd": ws_b.numel(), "kl_bwd": ws_k.numel(),
-                                "backward": ws_all.numel()},
+                                "backward": ws_all.numel(), "backward_in_passes": ws_w.numel()},
             "note": "outside the timed forward step; dkv / dk_I accumulate over calls"}
 
 

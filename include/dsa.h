@@ -104,7 +104,11 @@ typedef struct {
   int64_t wave_rows;           /* dsa_forward: rows per indexer/top-k wave; 0 = auto:
                                   as many as fit 256 MB of scores, rounded down to a
                                   multiple of 4 x the SM count; 1024 when not even
-                                  that many fit */
+                                  that many fit.  bf16 backward calls: with
+                                  0 < wave_rows < S_q, rows per pass (the passes
+                                  run one after the other, each within one
+                                  batch, and the workspace holds one pass); 0 or
+                                  >= S_q: one pass over all rows */
 } dsa_params;
 
 /* Library version as 10000*major + 100*minor + patch. */
@@ -227,10 +231,11 @@ int dsa_sparse_attn_fwd(const dsa_params *p, const void *q, const void *kv, cons
  *   bf16 path: DeepSeek head shapes only (H 128, d_qk 576, d_v 512) with
  *       topk <= 2048 and topk % 8 == 0, else DSA_ERR_UNSUPPORTED; q, kv, out,
  *       dout, dq, dkv and the workspace 16-byte aligned.  The workspace holds
- *       P and scale*dS for every (row, head, slot) as bf16 hi/lo pairs plus
- *       D, i.e. 1024 * rows * topk + 512 * rows + 256 bytes (34 GB at
- *       rows = 16384, topk = 2048); it must stay untouched until the call's
- *       kernels have finished on `stream`.
+ *       P and scale*dS for every (row, head, slot) of one pass as bf16 hi/lo
+ *       pairs plus D, i.e. 1024 * rows * topk + 512 * rows + 256 bytes with
+ *       rows = all B * S_q rows (34 GB at 16384 rows, topk = 2048) or, with
+ *       0 < wave_rows < S_q, rows = wave_rows (2.1 GB at 1024); it must stay
+ *       untouched until the call's kernels have finished on `stream`.
  */
 int dsa_sparse_attn_bwd(const dsa_params *p, const void *q, const void *kv, const int32_t *idx,
                         const void *out, const void *dout, const float *softmax_max,
@@ -253,7 +258,8 @@ int dsa_sparse_attn_bwd(const dsa_params *p, const void *q, const void *kv, cons
  *       d_I 128, else DSA_ERR_UNSUPPORTED; q, kv, k_I, dk_I and the workspace
  *       16-byte aligned, dq_I 4-byte aligned, topk <= 2048.  The workspace
  *       holds the head-summed attention probabilities, fp32:
- *       4 * rows * topk + 256 bytes.
+ *       4 * rows * topk + 256 bytes (rows: one pass, as for
+ *       dsa_sparse_attn_bwd).
  */
 int dsa_indexer_kl_loss_bwd(const dsa_params *p, const void *q, const void *kv, const void *q_I,
                             const void *k_I, const void *w, const int32_t *idx,

@@ -4,7 +4,9 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "dsa_common.cuh"
 
@@ -325,6 +327,46 @@ static int indexer_topk_waves(const dsa_params* p, const Shape& s, const void* q
 
 using namespace dsa;
 
+// bf16 backward in row passes: with 0 < wave_rows < S_q the rows run in
+// passes of at most wave_rows rows of one batch, one after the other on the
+// stream, and the workspace holds one pass (its P / dS pairs).  Rows are
+// independent and dkv, dk_I and the loss accumulate, so the passes give the
+// one-pass results (up to the order of the accumulating atomics).
+static long long bwd_pass_rows(const dsa_params* p) {
+  return (p->wave_rows > 0 && p->wave_rows < p->S_q) ? p->wave_rows : 0;
+}
+static Shape bwd_ws_shape(const dsa_params* p, const Shape& s) {
+  Shape t = s;
+  if (const long long W = bwd_pass_rows(p)) {
+    t.B = 1;
+    t.S_q = (int)W;
+  }
+  return t;
+}
+// f(shape, first flattened row, batch) for each pass; one call when unsplit
+template <typename F>
+static int bwd_passes(const dsa_params* p, const Shape& s, F f) {
+  const long long W = bwd_pass_rows(p);
+  if (W == 0) return f(s, 0LL, 0LL);
+  for (long long b = 0; b < s.B; ++b)
+    for (long long r0 = 0; r0 < s.S_q; r0 += W) {
+      const long long n = std::min(W, (long long)s.S_q - r0);
+      Shape t = s;
+      t.B = 1;
+      t.S_q = (int)n;
+      if (s.q_row_index) t.q_row_index = s.q_row_index + b * s.S_q + r0;
+      else t.q_row_offset = s.q_row_offset + r0;
+      const int rc = f(t, b * s.S_q + r0, b);
+      if (rc) return rc;
+    }
+  return DSA_OK;
+}
+template <typename T>
+static T* elem_off(T* ptr, long long elems, size_t esz) {
+  using B = typename std::conditional<std::is_const<T>::value, const uint8_t, uint8_t>::type;
+  return reinterpret_cast<T*>(reinterpret_cast<B*>(ptr) + elems * (long long)esz);
+}
+
 extern "C" {
 
 int dsa_version(void) { return 100; }
@@ -339,10 +381,11 @@ size_t dsa_workspace_size(const dsa_params* p, int which) {
     return bytes;
   }
   if (which == DSA_CALL_INDEXER_TOPK) return fused_topk_shape(p) ? fused_topk_workspace(p) : 0;
-  if (which == DSA_CALL_ATTN_BWD && tc_bwd_shape(p)) return bwd_tc_workspace(s);
-  if (which == DSA_CALL_KL_BWD && tc_bwd_shape(p) && tc_indexer_shape(p)) return kl_tc_workspace(s);
+  const Shape sw = bwd_ws_shape(p, s);  // one pass of the bf16 backward
+  if (which == DSA_CALL_ATTN_BWD && tc_bwd_shape(p)) return bwd_tc_workspace(sw);
+  if (which == DSA_CALL_KL_BWD && tc_bwd_shape(p) && tc_indexer_shape(p)) return kl_tc_workspace(sw);
   if (which == DSA_CALL_BACKWARD) {
-    if (tc_bwd_shape(p) && tc_indexer_shape(p)) return bwd_tc_workspace(s) + kl_tc_workspace(s);
+    if (tc_bwd_shape(p) && tc_indexer_shape(p)) return bwd_tc_workspace(sw) + kl_tc_workspace(sw);
     const size_t a = dsa_workspace_size(p, DSA_CALL_ATTN_BWD), b = dsa_workspace_size(p, DSA_CALL_KL_BWD);
     return a > b ? a : b;  // the exact path runs the two passes one after the other
   }
@@ -463,8 +506,13 @@ int dsa_sparse_attn_bwd(const dsa_params* p, const void* q, const void* kv, cons
     if (!workspace || !aligned16(workspace)) return DSA_ERR_WORKSPACE;
     DevCtx c;
     if (!dev_ctx(&c)) return DSA_ERR_CUDA;
-    return launch_attn_bwd_tc(s, q, kv, idx, out, dout, softmax_max, softmax_sum, dq, dkv,
-                              workspace, c, (cudaStream_t)stream, nullptr);
+    const long long H = p->H, dqk = p->d_qk, dv = p->d_v, Sk = p->S_k, k = p->topk;
+    return bwd_passes(p, s, [&](const Shape& t, long long r, long long b) {
+      return launch_attn_bwd_tc(t, elem_off(q, r * H * dqk, 2), elem_off(kv, b * Sk * dqk, 2), idx + r * k,
+                                elem_off(out, r * H * dv, 2), elem_off(dout, r * H * dv, 2),
+                                softmax_max + r * H, softmax_sum + r * H, elem_off(dq, r * H * dqk, 2),
+                                dkv + b * Sk * dqk, workspace, c, (cudaStream_t)stream, nullptr);
+    });
   }
   if (p->dtype == DSA_BF16 || simt_smem_attn_bwd(s) > 200 * 1024) return DSA_ERR_UNSUPPORTED;
   if (dsa_workspace_size(p, DSA_CALL_ATTN_BWD) > 0 && !aligned16(workspace)) return DSA_ERR_WORKSPACE;
@@ -492,8 +540,14 @@ int dsa_indexer_kl_loss_bwd(const dsa_params* p, const void* q, const void* kv, 
     if (!workspace || !aligned16(workspace)) return DSA_ERR_WORKSPACE;
     DevCtx c;
     if (!dev_ctx(&c)) return DSA_ERR_CUDA;
-    return launch_kl_bwd_tc(s, q, kv, q_I, k_I, w, idx, softmax_max, softmax_sum, loss, dq_I, dk_I,
-                            dw, workspace, c, (cudaStream_t)stream);
+    const long long H = p->H, dqk = p->d_qk, Sk = p->S_k, k = p->topk, HI = p->H_I, dI = p->d_I;
+    return bwd_passes(p, s, [&](const Shape& t, long long r, long long b) {
+      return launch_kl_bwd_tc(t, elem_off(q, r * H * dqk, 2), elem_off(kv, b * Sk * dqk, 2),
+                              elem_off(q_I, r * HI * dI, 2), elem_off(k_I, b * Sk * dI, 2),
+                              elem_off(w, r * HI, 2), idx + r * k, softmax_max + r * H,
+                              softmax_sum + r * H, loss, elem_off(dq_I, r * HI * dI, 2),
+                              dk_I + b * Sk * dI, dw + r * HI, workspace, c, (cudaStream_t)stream);
+    });
   }
   if (p->dtype == DSA_BF16 || simt_smem_kl(s) > 200 * 1024) return DSA_ERR_UNSUPPORTED;
   if (dsa_workspace_size(p, DSA_CALL_KL_BWD) > 0 && !aligned16(workspace)) return DSA_ERR_WORKSPACE;
@@ -522,8 +576,17 @@ int dsa_backward(const dsa_params* p, const void* q, const void* kv, const int32
     if (!workspace || !aligned16(workspace)) return DSA_ERR_WORKSPACE;
     DevCtx c;
     if (!dev_ctx(&c)) return DSA_ERR_CUDA;
-    return launch_dsa_bwd_tc(s, q, kv, idx, out, dout, softmax_max, softmax_sum, q_I, k_I, w, dq,
-                             dkv, loss, dq_I, dk_I, dw, workspace, c, (cudaStream_t)stream);
+    const long long H = p->H, dqk = p->d_qk, dv = p->d_v, Sk = p->S_k, k = p->topk, HI = p->H_I,
+                    dI = p->d_I;
+    return bwd_passes(p, s, [&](const Shape& t, long long r, long long b) {
+      return launch_dsa_bwd_tc(t, elem_off(q, r * H * dqk, 2), elem_off(kv, b * Sk * dqk, 2), idx + r * k,
+                               elem_off(out, r * H * dv, 2), elem_off(dout, r * H * dv, 2),
+                               softmax_max + r * H, softmax_sum + r * H, elem_off(q_I, r * HI * dI, 2),
+                               elem_off(k_I, b * Sk * dI, 2), elem_off(w, r * HI, 2),
+                               elem_off(dq, r * H * dqk, 2), dkv + b * Sk * dqk, loss,
+                               elem_off(dq_I, r * HI * dI, 2), dk_I + b * Sk * dI, dw + r * HI,
+                               workspace, c, (cudaStream_t)stream);
+    });
   }
   rc = dsa_sparse_attn_bwd(p, q, kv, idx, out, dout, softmax_max, softmax_sum, dq, dkv, workspace,
                            stream);

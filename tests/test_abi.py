@@ -105,6 +105,19 @@ def test_backward_workspace_sizes():
     # the fused backward: the attention backward's workspace, then the KL target
     assert dsa.workspace_size(p, dsa.DSA_CALL_BACKWARD) == \
         (4 * rh * k * 2 + rh * 4 + 256) + (rows * k * 4 + 256)
+    # row passes (0 < wave_rows < S_q): the workspace holds one pass of
+    # wave_rows rows whatever B and S_q are; wave_rows >= S_q is one pass
+    for B, S_q, W in ((1, 24, 10), (3, 24, 10), (2, 100, 7)):
+        pw = dsa.make_params(B=B, S_q=S_q, S_k=16384, H=128, d_qk=576, d_v=512, H_I=64, d_I=128,
+                             topk=k, scale=0.5, dtype="bf16", wave_rows=W)
+        wh = W * 128
+        assert dsa.workspace_size(pw, dsa.DSA_CALL_ATTN_BWD) == 4 * wh * k * 2 + wh * 4 + 256
+        assert dsa.workspace_size(pw, dsa.DSA_CALL_KL_BWD) == W * k * 4 + 256
+        assert dsa.workspace_size(pw, dsa.DSA_CALL_BACKWARD) == \
+            (4 * wh * k * 2 + wh * 4 + 256) + (W * k * 4 + 256)
+    whole = dsa.make_params(B=1, S_q=rows, S_k=16384, H=128, d_qk=576, d_v=512, H_I=64, d_I=128,
+                            topk=k, scale=0.5, dtype="bf16", wave_rows=rows)
+    assert dsa.workspace_size(whole, dsa.DSA_CALL_ATTN_BWD) == dsa.workspace_size(p, dsa.DSA_CALL_ATTN_BWD)
     # a k that is not a multiple of 8 has no tensor-core backward
     odd = dsa.make_params(B=1, S_q=rows, S_k=16384, H=128, d_qk=576, d_v=512, H_I=64, d_I=128,
                           topk=2047, scale=0.5, dtype="bf16")

@@ -122,3 +122,57 @@ def test_backward_empty_rows_and_late_key_tiles():
                 idx[0, r, 256 - keep.size:] = keep
 
     _check(_run_case(wl, list(range(448)), edit))
+
+
+@pytest.mark.parametrize("B,wave,index", [(1, 100, False), (2, 160, False), (1, 24, True)])
+def test_backward_in_row_passes(B, wave, index):
+    # 0 < wave_rows < S_q: the bf16 backward runs in passes of at most
+    # wave_rows rows of one batch, with a workspace for one pass.  Rows are
+    # independent and dkv, dk_I and the loss accumulate, so dq, dq_I and dw
+    # equal the one-pass call bit for bit and the accumulated outputs agree up
+    # to the order of the atomic additions.  Cases: ragged last pass, two
+    # batches, rows given by q_row_index (a context-parallel shard)
+    dsa = lib()
+    wl = dict(synth.v32(448, "passes"), topk=200, B=B)
+    S = wl["S"]
+    kw = {}
+    n = S
+    if index:
+        rows = np.sort(np.random.default_rng(7).choice(S, 64, replace=False)).astype(np.int32)
+        n = len(rows)
+        kw = dict(S_q=n, q_row_index=torch.as_tensor(rows, device=DEV))
+    x = {nm: v.to(DEV) for nm, v in synth.make_inputs(wl, with_dout=True, S_q=n).items()}
+    p_one = params(dsa, wl, **kw)
+    ws = torch.empty(dsa.workspace_size(p_one, dsa.DSA_CALL_FORWARD), dtype=torch.uint8, device=DEV)
+    idx = torch.empty(B, n, wl["topk"], dtype=torch.int32, device=DEV)
+    out = torch.empty(B, n, wl["H"], wl["d_v"], dtype=torch.bfloat16, device=DEV)
+    m = torch.empty(B, n, wl["H"], device=DEV)
+    l = torch.empty_like(m)
+    dsa.forward(p_one, x["q_I"], x["k_I"], x["w"], x["q"], x["kv"], idx, out, m, l, ws)
+
+    def run(p):
+        r = dict(dq=torch.empty(B, n, wl["H"], wl["d_qk"], dtype=torch.bfloat16, device=DEV),
+                 dkv=torch.zeros(B, S, wl["d_qk"], device=DEV), loss=torch.zeros(1, device=DEV),
+                 dqI=torch.empty(B, n, wl["H_I"], wl["d_I"], dtype=torch.bfloat16, device=DEV),
+                 dkI=torch.zeros(B, S, wl["d_I"], device=DEV),
+                 dw=torch.empty(B, n, wl["H_I"], device=DEV))
+        wsb = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_BACKWARD), dtype=torch.uint8, device=DEV)
+        dsa.backward(p, x["q"], x["kv"], idx, out, x["dO"], m, l, x["q_I"], x["k_I"], x["w"],
+                     r["dq"], r["dkv"], r["loss"], r["dqI"], r["dkI"], r["dw"], wsb)
+        r["dq2"] = torch.empty_like(r["dq"])
+        r["dkv2"] = torch.zeros_like(r["dkv"])
+        wsa = torch.empty(dsa.workspace_size(p, dsa.DSA_CALL_ATTN_BWD), dtype=torch.uint8, device=DEV)
+        dsa.sparse_attn_bwd(p, x["q"], x["kv"], idx, out, x["dO"], m, l, r["dq2"], r["dkv2"], wsa)
+        torch.cuda.synchronize()
+        assert dsa.get_status() == 0
+        return r, wsb.numel()
+
+    one, ws_one = run(p_one)
+    parts, ws_parts = run(params(dsa, wl, wave_rows=wave, **kw))
+    assert ws_parts < ws_one
+    for key in ("dq", "dqI", "dw", "dq2"):
+        assert torch.equal(parts[key], one[key]), key
+    for key in ("dkv", "dkI", "dkv2"):
+        ref = one[key]
+        torch.testing.assert_close(parts[key], ref, rtol=1e-5, atol=1e-6 * float(ref.abs().max()))
+    assert abs(float(parts["loss"]) - float(one["loss"])) <= 1e-5 * abs(float(one["loss"]))
