@@ -95,9 +95,9 @@ __device__ __forceinline__ void find_bin(TopkSmem& sm, int nbins, uint32_t k_rem
 
 // A row with n <= k visible keys takes all of them: out = 0, 1, ..., n-1,
 // then -1 (16-byte stores when the row allows them).
-__device__ __forceinline__ void write_prefix_rows(int32_t* out, int n, int k, int nt = TK_THREADS) {
+__device__ __forceinline__ void write_prefix_rows(int32_t* out, int n, int k, int nt, int tid) {
   if ((k & 3) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
-    for (int j = threadIdx.x; j < k / 4; j += nt) {
+    for (int j = tid; j < k / 4; j += nt) {
       const int b = 4 * j;
       const int4 v = make_int4(b < n ? b : -1, b + 1 < n ? b + 1 : -1, b + 2 < n ? b + 2 : -1,
                                b + 3 < n ? b + 3 : -1);
@@ -105,7 +105,7 @@ __device__ __forceinline__ void write_prefix_rows(int32_t* out, int n, int k, in
     }
     return;
   }
-  for (int j = threadIdx.x; j < k; j += nt) out[j] = j < n ? j : -1;
+  for (int j = tid; j < k; j += nt) out[j] = j < n ? j : -1;
 }
 
 // Radix passes shared by both variants.  KEYS(fn) must call fn(key) for every
@@ -149,9 +149,10 @@ __device__ __forceinline__ void radix_select(TopkSmem& sm, int k, ForEach for_ea
 // histogram, all cleared at the start, and the threshold search takes two
 // barriers.
 constexpr int TK_CAND = 4096;
-struct TopkRegSmem {
+template <int CAND>
+struct __align__(16) TopkRegSmemT {
   uint32_t hist[2 * TK_HIST + 256];  // pass 1 | pass 2 | pass 3
-  uint32_t cand[TK_CAND];            // keys of the threshold's pass-1 bin
+  uint32_t cand[CAND];               // keys of the threshold's pass-1 bin
   uint32_t ws[TK_WARPS];
   uint32_t bin, above, bin_count;
   uint32_t n_cand;  // candidate slots handed out so far (this row)
@@ -168,28 +169,56 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x, int lane) {
   return x;
 }
 
-// Exclusive scan of v over the NT threads of the block in thread order; one
-// barrier.  ws must not be written again before the next barrier every
-// thread passes.
-template <int NT>
-__device__ __forceinline__ uint32_t block_excl_scan_1b(uint32_t v, uint32_t* ws) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// A block runs GROUPS independent rows at a time, one per group of GT
+// consecutive threads; a group synchronises on named barrier 1 + grp (the
+// whole block's barrier when there is one group).
+template <int GROUPS, int GT>
+__device__ __forceinline__ void gsync(int grp) {
+  if constexpr (GROUPS == 1) {
+    __syncthreads();
+  } else {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(GT) : "memory");
+  }
+}
+template <int GROUPS, int GT>
+__device__ __forceinline__ bool gsync_or(int grp, bool v) {
+  if constexpr (GROUPS == 1) {
+    return __syncthreads_or(v) != 0;
+  } else {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, %2, %3, q;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(1 + grp), "r"(GT)
+        : "memory");
+    return r != 0;
+  }
+}
+
+// Exclusive scan of v over the GT threads of the group in thread order (tid =
+// index in the group); one barrier.  ws must not be written again before the
+// next barrier every thread of the group passes.
+template <int GT, int GROUPS>
+__device__ __forceinline__ uint32_t group_excl_scan_1b(uint32_t v, uint32_t* ws, int tid, int grp) {
+  const int lane = tid & 31, warp = tid >> 5;
   const uint32_t x = warp_incl_scan(v, lane);
   if (lane == 31) ws[warp] = x;
-  __syncthreads();
-  const uint32_t t = lane < NT / 32 ? ws[lane] : 0u;
+  gsync<GROUPS, GT>(grp);
+  const uint32_t t = lane < GT / 32 ? ws[lane] : 0u;
   const uint32_t ti = warp_incl_scan(t, lane);
   return __shfl_sync(0xffffffffu, ti - t, warp) + x - v;
 }
 
 // The bin b of hist[0..NB), counted from the top, with
 // count(> b) < k_rem <= count(>= b); result in sm.bin / above / bin_count.
-template <int NB, int NT>
-__device__ __forceinline__ void find_bin_2b(TopkRegSmem& sm, const uint32_t* hist, uint32_t k_rem) {
-  constexpr int PER = NB >= NT ? NB / NT : 1;
+template <int NB, int GT, int GROUPS, typename SM>
+__device__ __forceinline__ void find_bin_2b(SM& sm, const uint32_t* hist, uint32_t k_rem, int tid,
+                                            int grp) {
+  constexpr int PER = NB >= GT ? NB / GT : 1;
   static_assert(PER == 1 || PER % 4 == 0, "bins per thread");
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int hi = NB - (int)threadIdx.x * PER;  // this thread: bins [hi-PER, hi)
+  const int lane = tid & 31, warp = tid >> 5;
+  const int hi = NB - tid * PER;  // this thread: bins [hi-PER, hi)
   uint32_t local = 0;
   if constexpr (PER >= 4) {
 #pragma unroll
@@ -202,9 +231,9 @@ __device__ __forceinline__ void find_bin_2b(TopkRegSmem& sm, const uint32_t* his
   }
   const uint32_t x = warp_incl_scan(local, lane);
   if (lane == 31) sm.ws[warp] = x;
-  if (threadIdx.x == 0) sm.bin = 0, sm.above = 0, sm.bin_count = 0;
-  __syncthreads();
-  const uint32_t t = lane < NT / 32 ? sm.ws[lane] : 0u;
+  if (tid == 0) sm.bin = 0, sm.above = 0, sm.bin_count = 0;
+  gsync<GROUPS, GT>(grp);
+  const uint32_t t = lane < GT / 32 ? sm.ws[lane] : 0u;
   const uint32_t ti = warp_incl_scan(t, lane);
   uint32_t acc = __shfl_sync(0xffffffffu, ti - t, warp) + x - local;
   if (acc < k_rem && acc + local >= k_rem) {  // the one thread whose bins hold it
@@ -219,7 +248,7 @@ __device__ __forceinline__ void find_bin_2b(TopkRegSmem& sm, const uint32_t* his
       acc += h;
     }
   }
-  __syncthreads();
+  gsync<GROUPS, GT>(grp);
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int x, int y, int z,
@@ -240,40 +269,48 @@ __device__ __forceinline__ uint32_t shift_in_gt(uint32_t mask, uint32_t a, uint3
   return r;
 }
 
-// Persistent: CTA b takes rows b, b + gridDim.x, ...  When the scores are
-// reachable by TMA (tma_elems > 0: the first tma_elems columns of every row,
-// viewed as 128-byte lines) one thread loads the CTA's next row into a
-// shared-memory stage as soon as the current one has been read from it, so
-// the next row streams in while this one is selected.  The 128-byte swizzle
-// puts 16-byte piece g of a row at g ^ ((g >> 3) & 7), so the 8 lanes of a
-// quarter-warp reading their consecutive pieces hit distinct banks.
-template <int KPT, int NT>
+// Persistent: a CTA takes GROUPS rows at a time, one per group of GT = NT /
+// GROUPS threads (group grp of CTA b: rows GROUPS*b + grp, then + GROUPS *
+// gridDim.x, ...); two groups let one row's barrier phases overlap the
+// other's work.  When the scores are reachable by TMA (tma_elems > 0: the
+// first tma_elems columns of every row, viewed as 128-byte lines) one thread
+// of a group loads its next row into the group's shared-memory stage as soon
+// as the current one has been read from it, so the next row streams in while
+// this one is selected.  The 128-byte swizzle puts 16-byte piece g of a row
+// at g ^ ((g >> 3) & 7), so the 8 lanes of a quarter-warp reading their
+// consecutive pieces hit distinct banks.
+template <int KPT, int NT, int GROUPS>
 __global__ void __launch_bounds__(NT, TK_THREADS / NT)
     topk_reg_kernel(const __grid_constant__ CUtensorMap tm, Shape s, const float* __restrict__ scores,
                     long long ld, long long row_begin, long long rows, int32_t* __restrict__ idx,
                     DevCtx c, int tma_elems) {
   static_assert(KPT % 4 == 0 && KPT <= 32, "keys per thread");
+  constexpr int GT = NT / GROUPS;                     // threads per row
+  constexpr int CAND = GROUPS == 1 ? TK_CAND : TK_CAND / 2;
+  using Smem = TopkRegSmemT<CAND>;
   constexpr int C = KPT / 4;                          // 16-byte pieces per thread
   constexpr int BOX_ROWS = 32 * KPT < 256 ? 32 * KPT : 256;  // 128-byte lines per TMA box
   constexpr int BOX_ELEMS = BOX_ROWS * 32;
-  extern __shared__ uint8_t dyn_smem[];  // [align 1024] stage | TopkRegSmem
+  extern __shared__ uint8_t dyn_smem[];  // [align 1024] stage per group | Smem per group
   const uint32_t base = smem_u32(dyn_smem);
   uint8_t* aligned = dyn_smem + (((base + 1023u) & ~1023u) - base);
-  const float4* stage = reinterpret_cast<const float4*>(aligned);
-  // the row stage exists only in the 1024-thread form (the others load
+  const int grp = GROUPS == 1 ? 0 : (int)threadIdx.x / GT;
+  const int tid = (int)threadIdx.x - grp * GT;        // thread index in the group
+  // the row stages exist only in the 1024-thread forms (the others load
   // directly: two to four of them share an SM)
-  constexpr int STAGE_BYTES = NT == TK_THREADS ? NT * KPT * 4 : 0;
-  TopkRegSmem& sm = *reinterpret_cast<TopkRegSmem*>(aligned + STAGE_BYTES);
+  constexpr int STAGE_BYTES = NT == TK_THREADS ? GT * KPT * 4 : 0;
+  const float4* stage = reinterpret_cast<const float4*>(aligned + grp * STAGE_BYTES);
+  Smem& sm = reinterpret_cast<Smem*>(aligned + GROUPS * STAGE_BYTES)[grp];
   volatile int* abort_flag = &sm.abort_flag;
-  const uint32_t bar = smem_u32(&sm.bar), stage_u32 = smem_u32(aligned);
+  const uint32_t bar = smem_u32(&sm.bar), stage_u32 = smem_u32(aligned + grp * STAGE_BYTES);
   const int k = s.topk;
   // winners staged in shared memory and written as 16-byte pieces (every
   // row's output 16-byte aligned), in the forms that run several CTAs per SM:
   // with one CTA per SM the extra barrier costs more than the scattered
   // stores (measured per wave: 256 threads -4 us, 1024 threads +6-8 us)
-  const bool stage_out = NT < TK_THREADS && k <= TK_CAND && (k & 3) == 0 &&
+  const bool stage_out = GROUPS == 1 && NT < TK_THREADS && k <= CAND && (k & 3) == 0 &&
                          (reinterpret_cast<uintptr_t>(idx) & 15u) == 0;
-  const int e0 = threadIdx.x * KPT;  // this thread's first element of a row
+  const int e0 = tid * KPT;  // this thread's first element of a row
   const bool staged = tma_elems > 0 && e0 + KPT <= tma_elems;  // my keys come from the stage
   // 32-bit row -> position arithmetic when it fits (a 64-bit modulo is slow)
   const bool narrow = s.q_row_index == nullptr && row_begin + rows <= 0x7FFFFFFFll;
@@ -288,7 +325,7 @@ __global__ void __launch_bounds__(NT, TK_THREADS / NT)
   // than NT * KPT - KPT and no pass-2 candidate while the threshold's bin
   // holds fewer than NT keys, so the copy is issued off the barrier chain.
   auto issue = [&](long long rl) {  // stage row rl if it is selected from
-    if (threadIdx.x != NT - 1 || !loads_row(rl)) return;
+    if (tid != GT - 1 || !loads_row(rl)) return;
     const int nn = (int)row_len(rl);
     const int nbox = (min(nn, tma_elems) + BOX_ELEMS - 1) / BOX_ELEMS;
     fence_proxy_async_smem();  // the stage's earlier reads come before these writes
@@ -296,26 +333,27 @@ __global__ void __launch_bounds__(NT, TK_THREADS / NT)
     for (int bx = 0; bx < nbox; ++bx)
       tma_load_3d(stage_u32 + bx * BOX_ELEMS * 4, &tm, 0, bx * BOX_ROWS, (int)rl, bar);
   };
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     mbar_init(bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
   uint32_t phase = 0;
-  issue(blockIdx.x);
-  for (long long rl = blockIdx.x; rl < rows; rl += gridDim.x) {
+  const long long first = (long long)blockIdx.x * GROUPS + grp, step = (long long)gridDim.x * GROUPS;
+  issue(first);
+  for (long long rl = first; rl < rows; rl += step) {
     int32_t* out = idx + rl * (long long)k;
     const long long nl = row_len(rl);
     if (nl < 0) {
-      if (threadIdx.x == 0) set_status(c, DSA_ERR_INDEX);
-      write_prefix_rows(out, 0, k, NT);
-      issue(rl + gridDim.x);
+      if (tid == 0) set_status(c, DSA_ERR_INDEX);
+      write_prefix_rows(out, 0, k, GT, tid);
+      issue(rl + step);
       continue;
     }
     if (nl <= k) {
-      write_prefix_rows(out, (int)nl, k, NT);
-      issue(rl + gridDim.x);
+      write_prefix_rows(out, (int)nl, k, GT, tid);
+      issue(rl + step);
       continue;
     }
     const int n = (int)nl;
@@ -331,7 +369,7 @@ __global__ void __launch_bounds__(NT, TK_THREADS / NT)
     if (staged) {
 #pragma unroll
       for (int j = 0; j < C; ++j) {
-        const int g = threadIdx.x * C + j;
+        const int g = tid * C + j;
         const float4 v = stage[g ^ ((g >> 3) & 7)];
         key[4 * j] = ordered_key(v.x);
         key[4 * j + 1] = ordered_key(v.y);
@@ -347,9 +385,9 @@ __global__ void __launch_bounds__(NT, TK_THREADS / NT)
 #pragma unroll
       for (int q = 0; q < KPT; ++q) key[q] = q < nv ? ordered_key(__ldcs(src + e0 + q)) : 0u;
     }
-    for (int i = threadIdx.x; i < 2 * TK_HIST + 256; i += NT) sm.hist[i] = 0;
-    if (threadIdx.x == 0) sm.n_cand = 0;
-    if (__syncthreads_or(!ok)) return;  // a stage load that never landed: give up
+    for (int i = tid; i < 2 * TK_HIST + 256; i += GT) sm.hist[i] = 0;
+    if (tid == 0) sm.n_cand = 0;
+    if (gsync_or<GROUPS, GT>(grp, !ok)) return;  // a stage load that never landed: give up
     // pass 1: bits 31..20 of every key
     uint32_t* h1 = sm.hist;
     if (nv == KPT) {
@@ -360,8 +398,8 @@ __global__ void __launch_bounds__(NT, TK_THREADS / NT)
       for (int q = 0; q < KPT; ++q)
         if (q < nv) atomicAdd(&h1[key[q] >> 20], 1u);
     }
-    __syncthreads();
-    find_bin_2b<TK_HIST, NT>(sm, h1, (uint32_t)k);
+    gsync<GROUPS, GT>(grp);
+    find_bin_2b<TK_HIST, GT, GROUPS>(sm, h1, (uint32_t)k, tid, grp);
     uint32_t k_rem = (uint32_t)k - sm.above;
     const uint32_t b1 = sm.bin, c1 = sm.bin_count;
     // keys above bin b1 (all taken) and keys in it, as bit masks over q
@@ -375,7 +413,7 @@ __global__ void __launch_bounds__(NT, TK_THREADS / NT)
     if (lo1 == 0) eqm = 0xFFFFFFFFu;
     gtm = (__brev(gtm) >> (32 - KPT)) & vmask;
     eqm = (__brev(eqm) >> (32 - KPT)) & ~gtm & vmask;
-    if (c1 != k_rem && c1 <= (uint32_t)TK_CAND) {
+    if (c1 != k_rem && c1 <= (uint32_t)CAND) {
       // the c1 keys of bin b1 go to shared memory and the later passes run
       // over them alone; each thread's keys take consecutive slots (one
       // shared counter bumped once per warp), the order across threads is
@@ -389,30 +427,30 @@ __global__ void __launch_bounds__(NT, TK_THREADS / NT)
       uint32_t off = __shfl_sync(0xffffffffu, wbase, 31) + incl - mine;
       for (uint32_t m = eqm; m; m &= m - 1u) {
         const int q = __ffs(m) - 1;
-        const int g = threadIdx.x * C + (q >> 2);
+        const int g = tid * C + (q >> 2);
         const float v = staged ? reinterpret_cast<const float*>(stage + (g ^ ((g >> 3) & 7)))[q & 3]
                                : src[e0 + q];
         sm.cand[off++] = ordered_key(v);
       }
-      __syncthreads();  // candidates complete; the stage is free
-      issue(rl + gridDim.x);
+      gsync<GROUPS, GT>(grp);  // candidates complete; the stage is free
+      issue(rl + step);
       uint32_t* h2 = sm.hist + TK_HIST;
-      for (uint32_t i = threadIdx.x; i < c1; i += NT)
+      for (uint32_t i = tid; i < c1; i += GT)
         atomicAdd(&h2[(sm.cand[i] >> 8) & 0xFFFu], 1u);
-      __syncthreads();
-      find_bin_2b<TK_HIST, NT>(sm, h2, k_rem);
+      gsync<GROUPS, GT>(grp);
+      find_bin_2b<TK_HIST, GT, GROUPS>(sm, h2, k_rem, tid, grp);
       k_rem -= sm.above;
       uint32_t tp = (b1 << 12) | sm.bin;
       int sh = 8;
       if (sm.bin_count != k_rem) {
         uint32_t* h3 = sm.hist + 2 * TK_HIST;
         const uint32_t b2 = sm.bin;
-        for (uint32_t i = threadIdx.x; i < c1; i += NT) {
+        for (uint32_t i = tid; i < c1; i += GT) {
           const uint32_t kk = sm.cand[i];
           if (((kk >> 8) & 0xFFFu) == b2) atomicAdd(&h3[kk & 0xFFu], 1u);
         }
-        __syncthreads();
-        find_bin_2b<256, NT>(sm, h3, k_rem);
+        gsync<GROUPS, GT>(grp);
+        find_bin_2b<256, GT, GROUPS>(sm, h3, k_rem, tid, grp);
         k_rem -= sm.above;
         sh = 0;
         tp = (tp << 8) | sm.bin;
@@ -430,16 +468,16 @@ __global__ void __launch_bounds__(NT, TK_THREADS / NT)
       gtm |= cgt;
       eqm = ceq;
     } else if (c1 != k_rem) {
-      // more than TK_CAND keys share the bin (heavy ties): passes over registers
-      issue(rl + gridDim.x);
+      // more than CAND keys share the bin (heavy ties): passes over registers
+      issue(rl + step);
       uint32_t tp = b1;
       int sh = 20;
       uint32_t* h2 = sm.hist + TK_HIST;
 #pragma unroll
       for (int q = 0; q < KPT; ++q)
         if (q < nv && key[q] - lo1 < (1u << 20)) atomicAdd(&h2[(key[q] >> 8) & 0xFFFu], 1u);
-      __syncthreads();
-      find_bin_2b<TK_HIST, NT>(sm, h2, k_rem);
+      gsync<GROUPS, GT>(grp);
+      find_bin_2b<TK_HIST, GT, GROUPS>(sm, h2, k_rem, tid, grp);
       k_rem -= sm.above;
       sh = 8;
       tp = (tp << 12) | sm.bin;
@@ -449,8 +487,8 @@ __global__ void __launch_bounds__(NT, TK_THREADS / NT)
 #pragma unroll
         for (int q = 0; q < KPT; ++q)
           if (q < nv && key[q] - lo2 < 256u) atomicAdd(&h3[key[q] & 0xFFu], 1u);
-        __syncthreads();
-        find_bin_2b<256, NT>(sm, h3, k_rem);
+        gsync<GROUPS, GT>(grp);
+        find_bin_2b<256, GT, GROUPS>(sm, h3, k_rem, tid, grp);
         k_rem -= sm.above;
         sh = 0;
         tp = (tp << 8) | sm.bin;
@@ -465,11 +503,11 @@ __global__ void __launch_bounds__(NT, TK_THREADS / NT)
       gtm = cgt & vmask;
       eqm = ceq & ~cgt & vmask;
     } else {
-      issue(rl + gridDim.x);  // every key of bin b1 is taken
+      issue(rl + step);  // every key of bin b1 is taken
     }
     const uint32_t take_eq = k_rem;
-    const uint32_t p =
-        block_excl_scan_1b<NT>((uint32_t)__popc(gtm) | ((uint32_t)__popc(eqm) << 16), sm.ws);
+    const uint32_t p = group_excl_scan_1b<GT, GROUPS>(
+        (uint32_t)__popc(gtm) | ((uint32_t)__popc(eqm) << 16), sm.ws, tid, grp);
     uint32_t gt_b = p & 0xFFFFu, eq_b = p >> 16;
     // exactly k winners: they are placed in the candidate list (free once the
     // scan's barrier is passed: every thread has classified its candidates)
@@ -487,10 +525,10 @@ __global__ void __launch_bounds__(NT, TK_THREADS / NT)
       }
     }
     if (stage_out) {
-      __syncthreads();
+      gsync<GROUPS, GT>(grp);
       const int4* sv = reinterpret_cast<const int4*>(sm.cand);
       int4* ov = reinterpret_cast<int4*>(out);
-      for (int i = threadIdx.x; i < k / 4; i += NT) ov[i] = sv[i];
+      for (int i = tid; i < k / 4; i += GT) ov[i] = sv[i];
     }
   }
 }
@@ -508,12 +546,12 @@ __global__ void __launch_bounds__(TK_THREADS, 1)
   const long long pos = row_pos(s, row);
   if (pos < 0 || pos >= s.S_k) {
     if (threadIdx.x == 0) set_status(c, DSA_ERR_INDEX);
-    write_prefix_rows(out, 0, k);
+    write_prefix_rows(out, 0, k, TK_THREADS, threadIdx.x);
     return;
   }
   const int n = (int)pos + 1;
   if (n <= k) {
-    write_prefix_rows(out, n, k);
+    write_prefix_rows(out, n, k, TK_THREADS, threadIdx.x);
     return;
   }
   const float* src = scores + r_local * ld;
@@ -574,12 +612,12 @@ __global__ void __launch_bounds__(TK_THREADS, 1)
   const long long pos = row_pos(s, row);
   if (pos < 0 || pos >= s.S_k) {
     if (threadIdx.x == 0) set_status(c, DSA_ERR_INDEX);
-    write_prefix_rows(out, 0, k);
+    write_prefix_rows(out, 0, k, TK_THREADS, threadIdx.x);
     return;
   }
   const int n = (int)pos + 1;
   if (n <= k) {
-    write_prefix_rows(out, n, k);
+    write_prefix_rows(out, n, k, TK_THREADS, threadIdx.x);
     return;
   }
   const uint32_t m = cand_cnt[r_local] < (uint32_t)n ? cand_cnt[r_local] : (uint32_t)n;
@@ -664,14 +702,16 @@ int launch_topk(const Shape& s, const float* scores, long long ld, long long row
     return DSA_ERR_CUDA;
   // The longest row of this launch sizes the block.  Rows of up to 4096 keys
   // take 256-thread blocks, four rows per SM (measured per 1824-row wave:
-  // 45 us at n <= 3648); longer rows one 1024-thread block per SM, whose
-  // cost per row hardly depends on the row's length (the select's barrier
-  // phases dominate), so the keys are spread over all 1024 threads: 8 per
-  // thread up to 8192 keys (67-69 us per wave against 72-86 us for 256-thread
-  // blocks with 32 each), 16 up to 16384 (78-84 us against 103-106 us with
-  // 32), 32 beyond.  512-thread blocks, two rows per SM, measured slower than
-  // 1024 for 8K-16K keys (100-145 us per wave).  The 1024-thread form stages
-  // its next row by TMA.
+  // 45 us at n <= 3648).  Longer rows take one 1024-thread block per SM,
+  // whose cost per row hardly depends on the row's length (the select's
+  // barrier phases dominate): up to 16384 keys as two 512-thread groups with
+  // a row each (16 keys per thread up to 8192, 32 up to 16384), so one row's
+  // barrier phases overlap the other's work, beyond that one row over all
+  // 1024 threads (32 keys each).  Measured per wave: one row over 1024
+  // threads 67-69 us (8 keys per thread, 4K-8K keys) and 78-84 us (16 keys,
+  // 8K-16K keys); 256-thread blocks with 32 keys 72-86 us at 4K-8K keys;
+  // separate 512-thread blocks, two per SM, without the TMA stage 100-145 us
+  // at 8K-16K keys.  The 1024-thread blocks stage each group's next row by TMA.
   long long n_rows_max = max_n;
   if (s.q_row_index == nullptr) {
     const long long b0 = row_begin / s.S_q, b1 = (row_begin + rows - 1) / s.S_q;
@@ -680,10 +720,12 @@ int launch_topk(const Shape& s, const float* scores, long long ld, long long row
     if (n_rows_max < 1) n_rows_max = 1;
   }
   const int nt = n_rows_max <= 4096 ? 256 : 1024;
-  int kpt = n_rows_max <= 8192 ? 8 : n_rows_max <= 16384 ? 16 : 32;
+  const int groups = nt == TK_THREADS && n_rows_max <= 16384 ? 2 : 1;
+  int kpt = groups == 2 && n_rows_max <= 8192 ? 16 : 32;
   if (nt == 256) kpt = n_rows_max <= 1024 ? 4 : n_rows_max <= 2048 ? 8 : 16;
-  const long long per_sm = TK_THREADS / nt;
-  const int g = (int)(rows < per_sm * sms ? rows : per_sm * sms);
+  const long long per_sm = TK_THREADS / nt;                     // CTAs per SM
+  const long long units = (rows + groups - 1) / groups;         // row groups
+  const int g = (int)(units < per_sm * sms ? units : per_sm * sms);
   // TMA view of each row (1024-thread form): S_k / 32 lines of 32 floats (the
   // last S_k % 32 columns, if any, are read directly)
   CUtensorMap tm;
@@ -697,7 +739,9 @@ int launch_topk(const Shape& s, const float* scores, long long ld, long long row
       return DSA_ERR_CUDA;
     tma_elems = (max_n / 32) * 32;
   }
-  const size_t smem = 1024 + (nt == TK_THREADS ? (size_t)nt * kpt * 4 : 0) + sizeof(TopkRegSmem);
+  const size_t stage = nt == TK_THREADS ? (size_t)(nt / groups) * kpt * 4 : 0;
+  const size_t per_group = groups == 2 ? sizeof(TopkRegSmemT<TK_CAND / 2>) : sizeof(TopkRegSmemT<TK_CAND>);
+  const size_t smem = 1024 + groups * (stage + per_group);
   auto run = [&](auto kernel) -> int {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess ||
@@ -708,13 +752,15 @@ int launch_topk(const Shape& s, const float* scores, long long ld, long long row
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
   };
   if (nt == 256) {
-    if (kpt == 4) return run(topk_reg_kernel<4, 256>);
-    if (kpt == 8) return run(topk_reg_kernel<8, 256>);
-    return run(topk_reg_kernel<16, 256>);
+    if (kpt == 4) return run(topk_reg_kernel<4, 256, 1>);
+    if (kpt == 8) return run(topk_reg_kernel<8, 256, 1>);
+    return run(topk_reg_kernel<16, 256, 1>);
   }
-  if (kpt == 8) return run(topk_reg_kernel<8, 1024>);
-  if (kpt == 16) return run(topk_reg_kernel<16, 1024>);
-  return run(topk_reg_kernel<32, 1024>);
+  if (groups == 2) {
+    if (kpt == 16) return run(topk_reg_kernel<16, 1024, 2>);
+    return run(topk_reg_kernel<32, 1024, 2>);
+  }
+  return run(topk_reg_kernel<32, 1024, 1>);
 }
 
 }  // namespace dsa

@@ -81,10 +81,12 @@ def test_heavy_ties_long_row():
 def test_sized_blocks_offset_rows(S_k, values):
     # rows addressed by offset (no q_row_index), so the launch sizes its
     # blocks by the longest row: up to 4096 keys the 256-thread form (16 keys
-    # per thread), up to 8192 the 1024-thread form with 8, up to 16384 with
-    # 16.  With one value the threshold's bin holds every key (the passes run
-    # over registers once it exceeds the 4096-entry list), with 3 a third of
-    # them, with 1000 a few dozen to a few hundred, with 0 normal scores
+    # per thread), up to 8192 1024-thread blocks of two 512-thread groups
+    # with a row each (16 keys per thread), up to 16384 the same with 32.
+    # With one value the threshold's bin holds every key (the passes run over
+    # registers once it exceeds the candidate list: 4096 entries, 2048 per
+    # group), with 3 a third of them, with 1000 a few dozen to a few hundred,
+    # with 0 normal scores
     dsa = lib()
     k, rows = 2048, 96
     r0 = S_k - rows
