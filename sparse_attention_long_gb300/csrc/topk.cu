@@ -718,6 +718,18 @@ int launch_topk(const Shape& s, const float* scores, long long ld, long long row
     const long long pmax = s.q_row_offset + (b0 == b1 ? (row_begin + rows - 1) % s.S_q : s.S_q - 1);
     n_rows_max = pmax + 1 < max_n ? pmax + 1 : max_n;
     if (n_rows_max < 1) n_rows_max = 1;
+    // rows of one batch that cross 16384 keys: the rows up to 16384 keys go
+    // to the two-group form in a launch of their own (when they fill at
+    // least one round of it), the longer ones to the one-row form
+    const long long n0 = s.q_row_offset + row_begin % s.S_q + 1;  // the first row's keys
+    if (n_rows_max > 16384 && b0 == b1 && n0 <= 16384) {
+      const long long lo = 16384 - n0 + 1;
+      if (lo >= 2LL * sms && lo < rows) {
+        const int rc = launch_topk(s, scores, ld, row_begin, lo, idx, c, st);
+        if (rc != DSA_OK) return rc;
+        return launch_topk(s, scores + lo * ld, ld, row_begin + lo, rows - lo, idx + lo * s.topk, c, st);
+      }
+    }
   }
   const int nt = n_rows_max <= 4096 ? 256 : 1024;
   const int groups = nt == TK_THREADS && n_rows_max <= 16384 ? 2 : 1;

@@ -104,3 +104,27 @@ def test_sized_blocks_offset_rows(S_k, values):
     ref = topk_select(sc[None], np.arange(r0, r0 + rows)[None], k)[0]
     bad = np.nonzero((got.cpu().numpy() != ref).any(axis=1))[0]
     assert bad.size == 0, f"{bad.size} rows differ, first row {bad[:3]}"
+
+
+@pytest.mark.parametrize("values", [3, 0])
+def test_offset_rows_across_16k_keys(values):
+    # offset rows whose key counts run from 15985 to 16784: the launch sends
+    # the rows of up to 16384 keys to the two-group form and the rest to the
+    # one-row form, as two launches over the same output
+    dsa = lib()
+    S_k, k, rows = 32768, 2048, 800
+    r0 = 16384 - 400
+    p = dsa.make_params(B=1, S_q=S_k, S_k=S_k, H=1, d_qk=8, d_v=8, H_I=1, d_I=8, topk=k, scale=1.0,
+                        dtype="fp32")
+    rng = np.random.default_rng(values + 17)
+    if values:
+        sc = rng.integers(0, values, size=(rows, S_k)).astype(np.float32)
+    else:
+        sc = synth.normal((rows, S_k), 13, seed=4, dtype=torch.float32).numpy() * 8.0
+    got = torch.full((rows, k), -7, dtype=torch.int32, device=DEV)
+    dsa.topk(p, torch.as_tensor(sc, device=DEV), r0, rows, got)
+    torch.cuda.synchronize()
+    assert dsa.get_status() == 0
+    ref = topk_select(sc[None], np.arange(r0, r0 + rows)[None], k)[0]
+    bad = np.nonzero((got.cpu().numpy() != ref).any(axis=1))[0]
+    assert bad.size == 0, f"{bad.size} rows differ, first row {bad[:3]}"
